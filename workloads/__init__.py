@@ -1,0 +1,505 @@
+"""Seeded synthetic inputs for the paged KV cache decode path.
+
+This module only *draws* inputs: token contents, context lengths, physical block
+pools, block tables, slot mappings and the event scripts of the sharing workloads.
+It holds none of the attention, scatter, copy or allocation arithmetic. The CPU
+oracle (``oracle/``) and the CUDA library (``paged_kv_cache_261_gb300``) both
+consume what it makes; neither is imported here.
+
+Token contents come from a counter-based generator. Element ``e`` of the row that
+tensor ``tid`` (K, V or q) holds for content key ``key`` at position ``pos`` is a
+pure integer function of ``(seed, tid, key, pos, e)``. The value is the sum of
+twelve 4-bit uniforms, centred and divided by 16: an Irwin-Hall stand-in for
+N(0, 1) with standard deviation 0.998 and range [-5.625, 5.625]. Every value is a
+multiple of 1/16 with at most 7 significant bits, so it is exact in fp32, fp16 and
+bf16 and the storage dtype needs no rounding step. The same code runs on numpy
+arrays and on torch tensors (host or device) and yields identical bits on both,
+which lets a test regenerate on the host exactly the rows that were generated on
+the device.
+
+Shapes follow the cache layout ``[num_blocks, block_size, num_kv_heads,
+head_dim]``. A table entry of -1 marks an unused logical block.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+M32 = 0xFFFFFFFF
+
+TID_K = 0
+TID_V = 1
+TID_Q = 2
+
+DTYPES = ("f32", "f16", "bf16")
+
+
+# ---------------------------------------------------------------------------
+# counter-based generator (numpy or torch, int64 arithmetic only)
+# ---------------------------------------------------------------------------
+
+def _is_torch(x) -> bool:
+    return type(x).__module__.startswith("torch")
+
+
+def _mix32(x):
+    """32-bit integer finaliser on int64 arrays holding values in [0, 2**32).
+
+    Every product stays below 2**59, so int64 never overflows and numpy and
+    torch give the same bits."""
+    x = (((x >> 16) ^ x) * 0x045D9F3B) & M32
+    x = (((x >> 16) ^ x) * 0x045D9F3B) & M32
+    return (x >> 16) ^ x
+
+
+def _mix_scalar(v: int) -> int:
+    v &= M32
+    v = (((v >> 16) ^ v) * 0x045D9F3B) & M32
+    v = (((v >> 16) ^ v) * 0x045D9F3B) & M32
+    return (v >> 16) ^ v
+
+
+def _irwin_hall(keys):
+    """keys: int64 array in [0, 2**32). Returns float32 values in [-5.625, 5.625]."""
+    a = _mix32(keys)
+    b = _mix32(keys ^ 0x5BD1E995)
+    s = a & 15
+    for i in range(1, 8):
+        s = s + ((a >> (4 * i)) & 15)
+    for i in range(4):
+        s = s + ((b >> (4 * i)) & 15)
+    s = s - 90
+    if _is_torch(s):
+        import torch
+        return s.to(torch.float32) / 16.0
+    return s.astype(np.float32) / np.float32(16.0)
+
+
+def content_rows(seed: int, tid: int, keys, positions, row_elems: int):
+    """Rows of token contents.
+
+    keys, positions: int64 arrays (numpy or torch) of equal length n.
+    Returns float32 [n, row_elems] on the same library/device as ``keys``.
+    """
+    h = _mix_scalar(seed * 0x9E3779B1 + tid * 0x7FEB352D)
+    r = _mix32(((_mix32((keys + h) & M32)) + positions * 0x2C1B3C6D) & M32)
+    if _is_torch(keys):
+        import torch
+        e = torch.arange(row_elems, dtype=torch.int64, device=keys.device)
+    else:
+        e = np.arange(row_elems, dtype=np.int64)
+    ek = (e * 0x297A2D39) & M32
+    return _irwin_hall(r[:, None] ^ ek[None, :])
+
+
+# ---------------------------------------------------------------------------
+# bf16 / f16 storage helpers (bit containers; values are already exact)
+# ---------------------------------------------------------------------------
+
+def to_storage_numpy(x: np.ndarray, dtype: str) -> np.ndarray:
+    """float32 values (exact in the target dtype) -> numpy array holding the bits.
+
+    f32 -> float32, f16 -> float16, bf16 -> uint16 bit patterns."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == "f32":
+        return x
+    if dtype == "f16":
+        return x.astype(np.float16)
+    if dtype == "bf16":
+        u = x.view(np.uint32)
+        if np.any(u & 0xFFFF):
+            raise ValueError("value not exactly representable in bf16")
+        return (u >> 16).astype(np.uint16)
+    raise ValueError(dtype)
+
+
+def storage_to_float64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Inverse of to_storage_numpy (exact)."""
+    if dtype == "bf16":
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def torch_dtype(dtype: str):
+    import torch
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+@dataclass
+class DecodeWorkload:
+    """One decode batch: per-sequence contexts laid out through block tables.
+
+    Sequence b holds positions [0, context_lens[b]). Its content at position pos
+    comes from key prefix_key[b] when pos < prefix_len[b], else from own_key[b]
+    (the shared-prefix workload shares prompt contents across samples).
+    The newest token (pos = context_lens[b] - 1) is the one the step writes with
+    paged_kv_write; slot_mapping[b] is its slot, or -1 when context_lens[b] == 0.
+    """
+    name: str
+    seed: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    dtype: str
+    scale: float
+    q_mult: float
+    context_lens: np.ndarray          # int32 [B]
+    block_tables: np.ndarray          # int32 [B, MB]
+    slot_mapping: np.ndarray          # int32 [B]
+    own_key: np.ndarray               # int64 [B]
+    prefix_key: np.ndarray            # int64 [B]
+    prefix_len: np.ndarray            # int64 [B]
+    extra_write_slots: np.ndarray | None = None   # int32 [T] (mixed serving step)
+    extra_write_key0: int = 1 << 24
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.num_seqs else 0
+
+    @property
+    def row_elems(self) -> int:
+        return self.num_kv_heads * self.head_dim
+
+    def content_keys(self, seq_idx, positions):
+        """Content key per (seq, pos); arrays of the same library."""
+        if _is_torch(positions):
+            import torch
+            dev = positions.device
+            own = torch.as_tensor(self.own_key, device=dev)[seq_idx]
+            pk = torch.as_tensor(self.prefix_key, device=dev)[seq_idx]
+            pl = torch.as_tensor(self.prefix_len, device=dev)[seq_idx]
+            return torch.where(positions < pl, pk, own)
+        own = self.own_key[seq_idx]
+        return np.where(positions < self.prefix_len[seq_idx], self.prefix_key[seq_idx], own)
+
+    def kv_rows(self, tid: int, seq_idx, positions):
+        """float32 [n, num_kv_heads*head_dim] rows for (seq_idx[i], positions[i])."""
+        keys = self.content_keys(seq_idx, positions)
+        return content_rows(self.seed, tid, keys, positions, self.row_elems)
+
+    def q_values(self, like=None):
+        """float32 [B, H, D] queries (q_mult applied; exact in every dtype)."""
+        B, H, D = self.num_seqs, self.num_heads, self.head_dim
+        if like is not None and _is_torch(like):
+            import torch
+            keys = torch.as_tensor(self.own_key, device=like.device)
+            pos = torch.zeros_like(keys)
+        else:
+            keys = self.own_key.astype(np.int64)
+            pos = np.zeros_like(keys)
+        rows = content_rows(self.seed, TID_Q, keys, pos, H * D)
+        return (rows * self.q_mult).reshape(B, H, D)
+
+    def newest_kv(self, like=None):
+        """float32 ([B, Hk, D], [B, Hk, D]): K and V rows of each newest token.
+        Rows of sequences with context 0 are zero (their slot is -1)."""
+        ctx = self.context_lens.astype(np.int64)
+        pos = np.maximum(ctx - 1, 0)
+        idx = np.arange(self.num_seqs, dtype=np.int64)
+        if like is not None and _is_torch(like):
+            import torch
+            idx_t = torch.as_tensor(idx, device=like.device)
+            pos_t = torch.as_tensor(pos, device=like.device)
+            k = self.kv_rows(TID_K, idx_t, pos_t)
+            v = self.kv_rows(TID_V, idx_t, pos_t)
+            live = torch.as_tensor(ctx > 0, device=like.device)[:, None]
+            k = torch.where(live, k, torch.zeros_like(k))
+            v = torch.where(live, v, torch.zeros_like(v))
+        else:
+            k = self.kv_rows(TID_K, idx, pos)
+            v = self.kv_rows(TID_V, idx, pos)
+            k[ctx == 0] = 0
+            v[ctx == 0] = 0
+        shp = (self.num_seqs, self.num_kv_heads, self.head_dim)
+        return k.reshape(shp), v.reshape(shp)
+
+    def extra_write_rows(self, like=None):
+        """K, V rows [T, Hk, D] of the mixed serving step's extra tokens."""
+        T = int(self.extra_write_slots.shape[0])
+        keys = np.arange(T, dtype=np.int64) + self.extra_write_key0
+        pos = np.zeros(T, dtype=np.int64)
+        if like is not None and _is_torch(like):
+            import torch
+            keys = torch.as_tensor(keys, device=like.device)
+            pos = torch.as_tensor(pos, device=like.device)
+        k = content_rows(self.seed, TID_K, keys, pos, self.row_elems)
+        v = content_rows(self.seed, TID_V, keys, pos, self.row_elems)
+        shp = (T, self.num_kv_heads, self.head_dim)
+        return k.reshape(shp), v.reshape(shp)
+
+    # -- placement of the pre-step cache contents ---------------------------
+
+    def _positions(self, seqs, include_newest: bool):
+        """(seq_idx, pos) int64 arrays for the tokens the cache holds before the step."""
+        ctx = self.context_lens.astype(np.int64)[seqs]
+        n = ctx if include_newest else np.maximum(ctx - 1, 0)
+        seq_idx = np.repeat(np.asarray(seqs, dtype=np.int64), n)
+        starts = np.repeat(np.cumsum(n) - n, n)
+        pos = np.arange(int(n.sum()), dtype=np.int64) - starts
+        return seq_idx, pos
+
+    def _slots(self, seq_idx, pos):
+        bs = self.block_size
+        phys = self.block_tables[seq_idx, pos // bs].astype(np.int64)
+        if np.any(phys < 0):
+            raise ValueError("table entry missing for a live position")
+        return phys * bs + pos % bs
+
+    def fill_cache_torch(self, key_cache, value_cache, include_newest=False,
+                         seqs=None, chunk_tokens=1 << 16):
+        """Write the pre-step contents into device (or host) torch caches.
+
+        Uses plain torch indexing; the library under test is not involved."""
+        import torch
+        seqs = np.arange(self.num_seqs) if seqs is None else np.asarray(seqs)
+        seq_idx, pos = self._positions(seqs, include_newest)
+        slots = self._slots(seq_idx, pos)
+        kflat = key_cache.view(-1, self.row_elems)
+        vflat = value_cache.view(-1, self.row_elems)
+        dev = key_cache.device
+        for s in range(0, seq_idx.shape[0], chunk_tokens):
+            si = torch.as_tensor(seq_idx[s:s + chunk_tokens], device=dev)
+            pi = torch.as_tensor(pos[s:s + chunk_tokens], device=dev)
+            sl = torch.as_tensor(slots[s:s + chunk_tokens], device=dev)
+            kflat[sl] = self.kv_rows(TID_K, si, pi).to(key_cache.dtype)
+            vflat[sl] = self.kv_rows(TID_V, si, pi).to(value_cache.dtype)
+
+    def contiguous_kv(self, b: int, include_newest: bool = True):
+        """float32 ([ctx, Hk, D], [ctx, Hk, D]) for sequence b, in position order."""
+        ctx = int(self.context_lens[b])
+        n = ctx if include_newest else max(ctx - 1, 0)
+        seq_idx = np.full(n, b, dtype=np.int64)
+        pos = np.arange(n, dtype=np.int64)
+        shp = (n, self.num_kv_heads, self.head_dim)
+        return (self.kv_rows(TID_K, seq_idx, pos).reshape(shp),
+                self.kv_rows(TID_V, seq_idx, pos).reshape(shp))
+
+    def compact_host_view(self, seqs, rng_seed: int = 7, include_newest=False):
+        """A small host paged cache holding only ``seqs``.
+
+        The chosen sequences' logical blocks are placed on a fresh random
+        permutation of a pool just big enough for them. Returns a dict with
+        float32 caches, int32 block_tables/context_lens for the chosen rows and
+        the newest-token slots in the new pool."""
+        seqs = np.asarray(seqs, dtype=np.int64)
+        bs = self.block_size
+        ctx = self.context_lens.astype(np.int64)[seqs]
+        nb = (ctx + bs - 1) // bs
+        total = int(nb.sum())
+        perm = np.random.default_rng(rng_seed).permutation(max(total, 1)).astype(np.int32)
+        mb = max(int(nb.max()) if nb.size else 1, 1)
+        tables = np.full((seqs.shape[0], mb), -1, dtype=np.int32)
+        off = 0
+        for i, n in enumerate(nb):
+            tables[i, :n] = perm[off:off + n]
+            off += n
+        nblk = max(total, 1)
+        kc = np.zeros((nblk, bs, self.num_kv_heads, self.head_dim), np.float32)
+        vc = np.zeros_like(kc)
+        for i, b in enumerate(seqs):
+            k, v = self.contiguous_kv(int(b), include_newest=include_newest)
+            n = k.shape[0]
+            p = np.arange(n)
+            phys = tables[i, p // bs].astype(np.int64)
+            kc.reshape(-1, self.num_kv_heads, self.head_dim)[phys * bs + p % bs] = k
+            vc.reshape(-1, self.num_kv_heads, self.head_dim)[phys * bs + p % bs] = v
+        newest = np.full(seqs.shape[0], -1, np.int32)
+        for i, c in enumerate(ctx):
+            if c > 0:
+                newest[i] = tables[i, (c - 1) // bs] * bs + (c - 1) % bs
+        return dict(key_cache=kc, value_cache=vc, block_tables=tables,
+                    context_lens=ctx.astype(np.int32), slot_mapping=newest,
+                    num_blocks=nblk)
+
+    def algorithmic_bytes(self) -> dict:
+        """Bytes a decode step must move at minimum (K and V once per (seq, kv-head),
+        q in, out back, the table entries used and the lengths)."""
+        s = {"f32": 4, "f16": 2, "bf16": 2}[self.dtype]
+        ctx = self.context_lens.astype(np.int64)
+        nb = (ctx + self.block_size - 1) // self.block_size
+        kv = int(ctx.sum()) * self.num_kv_heads * self.head_dim * 2 * s
+        qo = 2 * self.num_seqs * self.num_heads * self.head_dim * s
+        meta = 4 * int(nb.sum()) + 4 * self.num_seqs
+        write = 2 * int((ctx > 0).sum()) * self.row_elems * s * 2 + 4 * self.num_seqs
+        return dict(kv=kv, qo=qo, meta=meta, decode=kv + qo + meta, write=write)
+
+
+def _tables_from_pool(ctx: np.ndarray, block_size: int, perm: np.ndarray, mb: int | None = None):
+    nb = (ctx.astype(np.int64) + block_size - 1) // block_size
+    if mb is None:
+        mb = max(int(nb.max()), 1)
+    tables = np.full((ctx.shape[0], mb), -1, dtype=np.int32)
+    off = 0
+    for b, n in enumerate(nb):
+        tables[b, :n] = perm[off:off + n]
+        off += n
+    return tables, off
+
+
+def _newest_slots(ctx, tables, bs):
+    out = np.full(ctx.shape[0], -1, np.int32)
+    for b, c in enumerate(ctx):
+        if c > 0:
+            out[b] = tables[b, (c - 1) // bs] * bs + (c - 1) % bs
+    return out
+
+
+def make_decode(name: str, seed: int, ctx: np.ndarray, num_heads: int, num_kv_heads: int,
+                head_dim: int, block_size: int, dtype: str, q_mult: float = 1.0,
+                pool_slack: float = 0.10, num_blocks: int | None = None,
+                extra_write: int = 0, mb: int | None = None, scale: float | None = None) -> DecodeWorkload:
+    """Generic builder: contexts ``ctx`` laid out on a shuffled pool."""
+    rng = np.random.default_rng(seed + 7919)
+    ctx = np.asarray(ctx, dtype=np.int32)
+    nb = (ctx.astype(np.int64) + block_size - 1) // block_size
+    need = int(nb.sum()) + (extra_write + block_size - 1) // block_size
+    if num_blocks is None:
+        num_blocks = max(int(math.ceil((1.0 + pool_slack) * need)), 1)
+    if num_blocks < need:
+        raise ValueError("pool too small")
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    tables, used = _tables_from_pool(ctx, block_size, perm, mb)
+    extra = None
+    if extra_write:
+        free_blocks = perm[used:].astype(np.int64)
+        free_slots = (free_blocks[:, None] * block_size + np.arange(block_size)[None, :]).reshape(-1)
+        extra = rng.choice(free_slots, extra_write, replace=False).astype(np.int32)
+    B = ctx.shape[0]
+    return DecodeWorkload(
+        name=name, seed=seed, num_heads=num_heads, num_kv_heads=num_kv_heads,
+        head_dim=head_dim, block_size=block_size, num_blocks=num_blocks, dtype=dtype,
+        scale=(1.0 / math.sqrt(head_dim)) if scale is None else scale, q_mult=q_mult,
+        context_lens=ctx, block_tables=tables,
+        slot_mapping=_newest_slots(ctx, tables, block_size),
+        own_key=np.arange(B, dtype=np.int64), prefix_key=np.zeros(B, np.int64),
+        prefix_len=np.zeros(B, np.int64), extra_write_slots=extra)
+
+
+# -- the five named workloads ------------------------------------------------
+
+def tiny_fp32(seed: int = 1001) -> DecodeWorkload:
+    """4 sequences of 5/17/33/64 tokens, 4 q heads = 4 kv heads, head_dim 64,
+    block_size 4, 64-block pool consumed in the order of a seeded permutation."""
+    rng = np.random.default_rng(seed)
+    ctx = np.array([5, 17, 33, 64], dtype=np.int32)
+    perm = rng.permutation(64).astype(np.int32)
+    tables, _ = _tables_from_pool(ctx, 4, perm)
+    B = 4
+    return DecodeWorkload(
+        name="tiny_fp32", seed=seed, num_heads=4, num_kv_heads=4, head_dim=64,
+        block_size=4, num_blocks=64, dtype="f32", scale=1.0 / 8.0, q_mult=1.0,
+        context_lens=ctx, block_tables=tables, slot_mapping=_newest_slots(ctx, tables, 4),
+        own_key=np.arange(B, dtype=np.int64), prefix_key=np.zeros(B, np.int64),
+        prefix_len=np.zeros(B, np.int64))
+
+
+def llama8b_decode(seed: int = 1002, num_seqs: int = 64, dtype: str = "bf16",
+                   block_size: int = 16) -> DecodeWorkload:
+    """Batch 64, 32 q heads / 8 kv heads, head_dim 128, bf16, block_size 16,
+    contexts uniform in [512, 4096], pool = total need + 10%, shuffled."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(512, 4097, size=num_seqs).astype(np.int32)
+    return make_decode("llama8b_decode", seed, ctx, 32, 8, 128, block_size, dtype)
+
+
+def long_context(seed: int = 1003, num_seqs: int = 8, dtype: str = "bf16") -> DecodeWorkload:
+    """Batch 8, contexts uniform in [32768, 131072], 64 q heads / 8 kv heads,
+    head_dim 128, bf16, block_size 16, q doubled for a peaky softmax."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(32768, 131073, size=num_seqs).astype(np.int32)
+    return make_decode("long_context", seed, ctx, 64, 8, 128, 16, dtype, q_mult=2.0)
+
+
+def mixed_serving(seed: int = 1005, block_size: int = 16, dtype: str = "bf16",
+                  num_seqs: int = 512, extra_write: int = 2048) -> DecodeWorkload:
+    """Batch 512 with lognormal contexts (median 600, sigma 1.0, clipped to
+    [16, 8192]) plus a 2048-token write to distinct random free slots. The
+    contexts and contents do not depend on block_size or dtype."""
+    rng = np.random.default_rng(seed)
+    ctx = np.clip(np.round(rng.lognormal(math.log(600.0), 1.0, size=num_seqs)), 16, 8192).astype(np.int32)
+    w = make_decode(f"mixed_serving_bs{block_size}_{dtype}", seed, ctx, 32, 8, 128,
+                    block_size, dtype, extra_write=extra_write)
+    return w
+
+
+@dataclass
+class SharedPrefixScript:
+    """Event script of the shared-prefix sampling workload.
+
+    num_prompts prompts of prompt_len tokens are prefilled, each is forked into
+    samples_per_prompt samples, then sample s appends private[s] earlier tokens
+    plus one current token. Samples append in index order."""
+    seed: int
+    num_prompts: int
+    samples_per_prompt: int
+    prompt_len: int
+    private: np.ndarray           # int64 [num_prompts * samples_per_prompt]
+    block_size: int
+    num_heads: int = 32
+    num_kv_heads: int = 8
+    head_dim: int = 128
+    dtype: str = "bf16"
+
+    @property
+    def num_samples(self) -> int:
+        return self.num_prompts * self.samples_per_prompt
+
+    def pool_blocks(self) -> int:
+        bs = self.block_size
+        prompt_blocks = (self.prompt_len + bs - 1) // bs
+        ctx = self.prompt_len + self.private + 1
+        private_blocks = ((ctx + bs - 1) // bs) - (self.prompt_len // bs)
+        need = self.num_prompts * prompt_blocks + int(private_blocks.sum())
+        return int(math.ceil(1.1 * need)) + 8
+
+    def workload(self, block_tables: np.ndarray, num_blocks: int) -> DecodeWorkload:
+        """The decode batch after every sample's current token, laid out on the
+        tables an allocator produced (rows in sample order)."""
+        S = self.num_samples
+        ctx = (self.prompt_len + self.private + 1).astype(np.int32)
+        prompt_of = np.arange(S, dtype=np.int64) // self.samples_per_prompt
+        return DecodeWorkload(
+            name="shared_prefix", seed=self.seed, num_heads=self.num_heads,
+            num_kv_heads=self.num_kv_heads, head_dim=self.head_dim,
+            block_size=self.block_size, num_blocks=num_blocks, dtype=self.dtype,
+            scale=1.0 / math.sqrt(self.head_dim), q_mult=1.0, context_lens=ctx,
+            block_tables=block_tables.astype(np.int32),
+            slot_mapping=_newest_slots(ctx, block_tables, self.block_size),
+            own_key=np.arange(S, dtype=np.int64) + (1 << 20),
+            prefix_key=prompt_of, prefix_len=np.full(S, self.prompt_len, np.int64))
+
+
+def shared_prefix(seed: int = 1004, num_prompts: int = 32, samples_per_prompt: int = 8,
+                  prompt_len: int = 1000, max_private: int = 256,
+                  block_size: int = 16) -> SharedPrefixScript:
+    rng = np.random.default_rng(seed)
+    private = rng.integers(0, max_private + 1, size=num_prompts * samples_per_prompt).astype(np.int64)
+    return SharedPrefixScript(seed=seed, num_prompts=num_prompts,
+                              samples_per_prompt=samples_per_prompt, prompt_len=prompt_len,
+                              private=private, block_size=block_size)
+
+
+WORKLOADS = {
+    "tiny_fp32": tiny_fp32,
+    "llama8b_decode": llama8b_decode,
+    "long_context": long_context,
+    "shared_prefix": shared_prefix,
+    "mixed_serving": mixed_serving,
+}
