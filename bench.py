@@ -1,0 +1,483 @@
+"""Benchmark of the paged decode step on GB300.
+
+One step = one pass of the hot path over one synthetic batch: the scatter of
+the step's new tokens into their cache slots (paged_kv_write), the
+copy-on-write block copies when the workload has them (copy_blocks), and decode
+attention over the paged cache (split-K partition kernel + merge kernel).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload llama8b_decode|long_context|mixed_serving|shared_prefix]
+
+Prints one JSON line (rank 0). ``value`` is algorithmic bytes per step (K and V
+of every context once, q, out, the table entries and lengths used, plus the
+written and copied rows) divided by the device time per step, in GB/s, summed
+over ranks (each rank runs its own replica of the workload: the path has no
+exchange step). The reference arm (--impl reference) times the CPU oracle on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode attn KV GB/s & tokens/s on 1×GB300; fraction of HBM peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_261_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+        ent = rec.get(workload)
+        if ent and ent.get("source_digest") == source_digest():
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pa_clocks_{os.getpid()}.csv")
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# device state of one workload
+# ---------------------------------------------------------------------------
+
+class Step:
+    """Device-resident inputs of one step and the calls that run it."""
+
+    def __init__(self, name: str, device):
+        import torch
+
+        import paged_kv_cache_261_gb300 as pa
+        self.pa = pa
+        self.name = name
+        self.device = device
+        self.copy_pairs = None
+        self.copy_bytes = 0
+        if name == "shared_prefix":
+            w, extra = self._shared_prefix_state()
+        else:
+            w = {"llama8b_decode": workloads.llama8b_decode, "long_context": workloads.long_context,
+                 "mixed_serving": workloads.mixed_serving}[name]()
+            extra = None
+        self.w = w
+        dt = workloads.torch_dtype(w.dtype)
+        self.tdtype = dt
+        shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+        self.kc = torch.zeros(shape, dtype=dt, device=device)
+        self.vc = torch.zeros(shape, dtype=dt, device=device)
+        w.fill_cache_torch(self.kc, self.vc, include_newest=False)
+        if name == "mixed_serving":
+            k, v = w.extra_write_rows(like=self.kc)
+            self.slots = torch.as_tensor(w.extra_write_slots, device=device)
+        else:
+            k, v = w.newest_kv(like=self.kc)
+            self.slots = torch.as_tensor(w.slot_mapping, device=device)
+        self.k_new = k.to(dt).contiguous()
+        self.v_new = v.to(dt).contiguous()
+        if name == "mixed_serving":
+            # the decode batch's own newest tokens are already in the cache
+            kn, vn = w.newest_kv(like=self.kc)
+            pa.paged_kv_write(kn.to(dt).contiguous(), vn.to(dt).contiguous(),
+                              torch.as_tensor(w.slot_mapping, device=device), self.kc, self.vc)
+        if extra is not None:
+            self.copy_pairs = torch.as_tensor(extra, device=device)
+            es = 2
+            self.copy_bytes = 2 * 2 * extra.shape[0] * w.block_size * w.row_elems * es
+        self.q = w.q_values(like=self.kc).to(dt).contiguous()
+        self.out = torch.empty_like(self.q)
+        self.bt = torch.as_tensor(w.block_tables, device=device)
+        self.cl = torch.as_tensor(w.context_lens, device=device)
+        self.max_ctx = int(w.context_lens.max())
+        self.ws = torch.empty(max(pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim,
+                                                            self.max_ctx, 0), 16),
+                              dtype=torch.uint8, device=device)
+        es = {"f32": 4, "f16": 2, "bf16": 2}[w.dtype]
+        ab = w.algorithmic_bytes()
+        self.decode_bytes = ab["decode"]
+        ntok = int(self.slots.shape[0])
+        self.write_bytes = 2 * 2 * ntok * w.row_elems * es + 4 * ntok
+        self.step_bytes = self.decode_bytes + self.write_bytes + self.copy_bytes
+        self.launches_per_step = 1 + (1 if self.copy_pairs is not None else 0) + 1 + (
+            1 if pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, self.max_ctx, 0) else 0)
+        torch.cuda.synchronize()
+
+    def _shared_prefix_state(self):
+        """Allocator replay of the shared-prefix workload (library allocator).
+        The step's copy_blocks duplicates each prompt's partial block into a
+        spare block per copy-on-write pair, which leaves the decode inputs intact."""
+        pa = self.pa
+        sc = workloads.shared_prefix()
+        npairs = (sc.samples_per_prompt - 1) * sc.num_prompts
+        nb = sc.pool_blocks() + npairs
+        a = pa.BlockAllocator(nb, sc.block_size)
+        pairs = []
+        for p in range(sc.num_prompts):
+            a.add_seq(p)
+            a.append(p, sc.prompt_len)
+            for j in range(sc.samples_per_prompt):
+                a.fork(p, 1000 + p * sc.samples_per_prompt + j)
+            a.free_seq(p)
+        for s in range(sc.num_samples):
+            _, pr = a.append(1000 + s, int(sc.private[s]) + 1)
+            pairs += pr.tolist()
+        spare = [a.alloc() for _ in range(len(pairs))]
+        ids = np.arange(sc.num_samples) + 1000
+        mb = max(len(a.block_table(int(i))) for i in ids)
+        tables, _ = a.export(ids, mb)
+        w = sc.workload(tables, nb)
+        extra = np.array([[src, dst] for (src, _), dst in zip(pairs, spare)], np.int32)
+        return w, extra
+
+    def run(self, ev=None):
+        """One step; ev = (start, end) CUDA events bracketing the decode call."""
+        pa = self.pa
+        if self.copy_pairs is not None:
+            pa.copy_blocks(self.kc, self.vc, self.copy_pairs)
+        pa.paged_kv_write(self.k_new, self.v_new, self.slots, self.kc, self.vc)
+        if ev is not None:
+            ev[0].record()
+        pa.paged_attention_decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl, self.w.scale,
+                                  max_context_len=self.max_ctx, workspace=self.ws)
+        if ev is not None:
+            ev[1].record()
+
+    def config(self):
+        w = self.w
+        return {"workload": self.name, "num_seqs": w.num_seqs, "num_heads": w.num_heads,
+                "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                "num_blocks": w.num_blocks, "context_total": int(w.context_lens.sum()),
+                "context_min": int(w.context_lens.min()), "context_max": int(w.context_lens.max()),
+                "written_tokens": int(self.slots.shape[0]),
+                "copied_blocks": 0 if self.copy_pairs is None else int(self.copy_pairs.shape[0]),
+                "partition_size": 512,
+                "l2": f"inputs larger than L2: {w.algorithmic_bytes()['kv'] / 1e9:.2f} GB of K/V read per step "
+                      f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, n_seqs: int):
+    """Host inputs of the oracle for the first n_seqs sequences (storage dtype)."""
+    seqs = np.arange(n_seqs)
+    view = w.compact_host_view(seqs, include_newest=False)
+    kc = workloads.to_storage_numpy(view["key_cache"], w.dtype)
+    vc = workloads.to_storage_numpy(view["value_cache"], w.dtype)
+    kn, vn = w.newest_kv()
+    row = w.row_elems
+    kn = workloads.to_storage_numpy(kn[seqs].reshape(-1, row), w.dtype)
+    vn = workloads.to_storage_numpy(vn[seqs].reshape(-1, row), w.dtype)
+    q = workloads.to_storage_numpy(w.q_values()[seqs], w.dtype)
+    return dict(kc=kc, vc=vc, kn=kn, vn=vn, q=q, slots=view["slot_mapping"], bt=view["block_tables"],
+                cl=view["context_lens"])
+
+
+def oracle_step(w, s, threads):
+    import oracle
+    kc, vc = s["kc"].copy(), s["vc"].copy()
+    oracle.kv_write(s["kn"], s["vn"], s["slots"], kc, vc, w.dtype)
+    return oracle.paged_attention(s["q"], kc, vc, s["bt"], s["cl"], w.scale, w.dtype, num_threads=threads)
+
+
+def sample_bytes(w, n_seqs):
+    es = {"f32": 4, "f16": 2, "bf16": 2}[w.dtype]
+    ctx = w.context_lens[:n_seqs].astype(np.int64)
+    nb = (ctx + w.block_size - 1) // w.block_size
+    return (int(ctx.sum()) * w.row_elems * 2 * es + 2 * n_seqs * w.num_heads * w.head_dim * es
+            + 4 * int(nb.sum()) + 4 * n_seqs + 2 * 2 * n_seqs * w.row_elems * es)
+
+
+def pick_sample(w, threads, budget_s):
+    """Largest prefix of sequences whose oracle pass fits the time budget."""
+    s1 = oracle_sample(w, 1)
+    t = time.perf_counter()
+    oracle_step(w, s1, threads)
+    dt = time.perf_counter() - t
+    per_tok = dt / max(int(w.context_lens[0]), 1)
+    # threads help once there are several (seq, kv-head) items
+    eff = max(1.0, min(threads, 8 * w.num_kv_heads) / 1.5)
+    n, tot = 0, 0.0
+    while n < w.num_seqs and tot + per_tok * w.context_lens[n] / eff <= budget_s:
+        tot += per_tok * w.context_lens[n] / eff
+        n += 1
+    return max(n, 1)
+
+
+def cpu_baseline(w, budget_s=15.0):
+    import oracle
+    threads = oracle.num_host_threads()
+    n = pick_sample(w, threads, budget_s)
+    s = oracle_sample(w, n)
+    t = time.perf_counter()
+    oracle_step(w, s, threads)
+    dt = time.perf_counter() - t
+    return {"value": sample_bytes(w, n) / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of {w.num_seqs} sequences ({int(w.context_lens[:n].sum())} context tokens): "
+                      f"newest-token scatter + decode, one pass, {dt:.2f} s"}
+
+
+def run_reference(args):
+    import oracle
+    name = args.workload
+    w = {"llama8b_decode": workloads.llama8b_decode, "long_context": workloads.long_context,
+         "mixed_serving": workloads.mixed_serving}.get(name, workloads.llama8b_decode)()
+    threads = oracle.num_host_threads()
+    budget = 90.0 / max(args.steps + args.warmup, 1)
+    n = pick_sample(w, threads, budget)
+    s = oracle_sample(w, n)
+    for _ in range(args.warmup):
+        oracle_step(w, s, threads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, s, threads)
+    dt = (time.perf_counter() - t) / max(args.steps, 1)
+    value = sample_bytes(w, n) / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": name, "num_seqs": w.num_seqs, "sampled_seqs": n},
+            "tokens_per_s": n / dt,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"first {n} of {w.num_seqs} sequences per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_261_gb300.build import build_library
+    if rank == 0 or world == 1:
+        build_library()
+    if world > 1:
+        dist.barrier()
+
+    st = Step(args.workload, device)
+    for _ in range(max(args.warmup, 3)):
+        st.run()
+    torch.cuda.synchronize()
+    if st.pa.get_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(args.steps):
+        st.run(evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler is not None else None
+    ms = t0.elapsed_time(t1)
+    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if world > 1:
+        tt = torch.tensor([ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / args.steps
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    e2e = run_e2e(st, args, device)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = hbm_peak()
+    achieved = st.decode_bytes / (decode_ms * 1e-3) / 1e9
+    value = world * st.step_bytes / (ms_step * 1e-3) / 1e9
+    w = st.w
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded counter-based generator)",
+        "config": st.config(),
+        "tokens_per_s": world * w.num_seqs / (ms_step * 1e-3),
+        "kv_tokens_per_s": world * int(w.context_lens.sum()) / (ms_step * 1e-3),
+        "hbm_fraction": value / world / peak,
+        "roofline": {"kernel": "paged_attention_decode (partition + merge kernels)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "algorithmic_bytes_per_launch": st.decode_bytes,
+                     "decode_ms": decode_ms, "traffic": recorded_traffic(args.workload)},
+        "e2e": e2e,
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(st: Step, args, device):
+    """Per step: pinned host -> device copies of the step's inputs (q, new K/V,
+    slot mapping, block tables, lengths), the write + decode calls, and a
+    device -> host copy of the output."""
+    import torch
+    n = max(min(args.steps, 500), 10)
+    host = {k: t.cpu().pin_memory() for k, t in
+            (("q", st.q), ("k", st.k_new), ("v", st.v_new), ("slots", st.slots), ("bt", st.bt), ("cl", st.cl))}
+    out_h = torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    dev_in = {k: torch.empty_like(t, device=device) for k, t in host.items()}
+
+    def one():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        pa = st.pa
+        if st.copy_pairs is not None:
+            pa.copy_blocks(st.kc, st.vc, st.copy_pairs)
+        pa.paged_kv_write(dev_in["k"], dev_in["v"], dev_in["slots"], st.kc, st.vc)
+        pa.paged_attention_decode(st.out, dev_in["q"], st.kc, st.vc, dev_in["bt"], dev_in["cl"], st.w.scale,
+                                  max_context_len=st.max_ctx, workspace=st.ws)
+        out_h.copy_(st.out, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"value": world * st.step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b_decode",
+                    choices=["llama8b_decode", "long_context", "mixed_serving", "shared_prefix"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,239 @@
+/*
+ * libpagedattn -- paged KV cache decode path for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI. Plain pointers and sizes only; no exceptions cross this boundary.
+ * Every entry point returns an int status (PA_OK = 0, negative on error).
+ *
+ * Sources (web pages, by title and section):
+ *  [P1] "PagedAttention实现" (ainanfeng.cn teaching version), sections
+ *       "Block定义" (one physical block holds block_size tokens' K and V),
+ *       "页表" (a per-sequence logical->physical block list) and
+ *       "PagedAttention管理器" (free list, reference counts, write_kv,
+ *       cow_write, free_sequence).
+ *  [P2] "CS349E lecture 7: 01_paged_attention.py", demo 1 (block-table
+ *       growth), demo 2 (paper eq. 4: block-wise scores, one softmax over the
+ *       whole context, block-wise V; equal to contiguous attention), demo 3
+ *       (prefix sharing with copy-on-write).
+ *  [P3] "04 - Paged Attention 实现进度", section A.2 (the five components) and
+ *       B.2 (slot_mapping [total_tokens], block_tables
+ *       [batch, max_blocks_per_seq], context_lens [batch]).
+ *
+ * Layouts (all row-major, C-contiguous):
+ *   key_cache, value_cache : [num_blocks, block_size, num_kv_heads, head_dim]
+ *   k, v (new tokens)      : [num_tokens, num_kv_heads, head_dim]
+ *   q, out                 : [num_seqs, num_heads, head_dim]
+ *   block_tables           : int32 [num_seqs, max_blocks_per_seq]
+ *   context_lens           : int32 [num_seqs]
+ *   slot_mapping           : int32 [num_tokens], slot = block * block_size + offset
+ *   src_dst_pairs          : int32 [num_pairs, 2]
+ * Query head h reads kv head h / (num_heads / num_kv_heads).
+ *
+ * Ownership and timing: the caller owns every buffer. Device pointers must be
+ * 16-byte aligned. Compute calls are asynchronous on the caller's CUDA stream
+ * (passed as void*, NULL = the legacy default stream); they validate shapes on
+ * the host and never read device data on the host. Index errors found on the
+ * device (a bad slot, block id, copy pair or context length) skip the bad
+ * access and set a bit in a per-device error word, read and cleared by
+ * pa_get_device_error(). No kernel traps or asserts.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes --------------------------------------------------------- */
+#define PA_OK                 0
+#define PA_ERR_INVALID_ARG   -1   /* bad shape, pointer, alignment or value      */
+#define PA_ERR_UNSUPPORTED   -2   /* valid but not implemented (e.g. head_dim)   */
+#define PA_ERR_OUT_OF_BLOCKS -3   /* allocator: free list too short              */
+#define PA_ERR_CUDA          -4   /* a CUDA runtime call failed                  */
+#define PA_ERR_DEVICE_INDEX  -5   /* pa_get_device_error: a device check fired   */
+#define PA_ERR_UNKNOWN_SEQ   -6   /* allocator: no such sequence id              */
+#define PA_ERR_WORKSPACE     -7   /* decode: workspace given but too small       */
+#define PA_ERR_EXISTS        -8   /* allocator: sequence id already present      */
+
+/* ---- element types -------------------------------------------------------- */
+#define PA_DTYPE_F32  0
+#define PA_DTYPE_F16  1
+#define PA_DTYPE_BF16 2
+
+/* ---- device error bits (pa_get_device_error) ------------------------------ */
+#define PA_DEVERR_SLOT       0x1u  /* slot not -1 and outside [0, NB*bs)          */
+#define PA_DEVERR_BLOCK_ID   0x2u  /* live table entry outside [0, num_blocks)    */
+#define PA_DEVERR_CONTEXT    0x4u  /* context_len < 0, > max_blocks_per_seq*bs,   */
+                                   /* or > max_context_len                        */
+#define PA_DEVERR_COPY_PAIR  0x8u  /* copy pair id outside [0, num_blocks)        */
+#define PA_DEVERR_WAIT       0x10u /* an internal pipeline wait hit its bound     */
+
+/* Name of a status code (static string). */
+const char *pa_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int pa_version(void);
+
+/*
+ * Scatter new tokens' K and V rows into their cache slots.
+ * [P1 write_kv: page = position / block_size, offset = position % block_size,
+ *  then the token's values are copied; P3 B.2: slot_mapping]
+ *
+ * Token t's row k[t] (num_kv_heads*head_dim elements) is copied to
+ * key_cache[slot / block_size, slot % block_size], and v[t] likewise, where
+ * slot = slot_mapping[t]. slot == -1 skips the token (padding). Any other slot
+ * outside [0, num_blocks*block_size) is skipped and sets PA_DEVERR_SLOT.
+ * Two tokens with the same slot are a caller error (the survivor is undefined).
+ * Requires num_kv_heads*head_dim*sizeof(dtype) to be a multiple of 16 bytes.
+ */
+int pa_paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping,
+                      int64_t num_tokens, void *key_cache, void *value_cache,
+                      int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                      int dtype, void *stream);
+
+/*
+ * Bytes of split-K workspace pa_paged_attention_decode needs for these sizes
+ * (0 when every sequence fits one partition). partition_size 0 = automatic.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                 int max_context_len, int partition_size);
+
+/*
+ * Single-query decode attention over the paged cache.
+ * [P2 demo 2, eq. 4: for each sequence and query head, scores against every
+ *  cached key are formed block by block through the block table, ONE softmax
+ *  is taken over the whole context, and V is accumulated block by block;
+ *  P3 B.2: block_tables, context_lens]
+ *
+ *   out[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . K[b,t,h/G,:]) * V[b,t,h/G,:]
+ *
+ * over t < context_lens[b]; position t lives in physical block
+ * block_tables[b, t / block_size] at offset t % block_size. Accumulation is
+ * fp32; out has q's dtype. context_lens[b] == 0 gives a zero row.
+ *
+ * Long contexts are split into partitions of partition_size tokens
+ * (0 = automatic, else a positive multiple of 128). Each partition keeps its
+ * running max, sum and unnormalised output in fp32 workspace, and a second
+ * kernel merges them. max_context_len is a host-side upper bound on every
+ * context_lens[b] (0 = max_blocks_per_seq * block_size); it sizes the grid
+ * and the workspace. A context above it, or above max_blocks_per_seq *
+ * block_size, or negative, sets PA_DEVERR_CONTEXT and is clamped to the
+ * covered range; a live table entry outside [0, num_blocks) sets
+ * PA_DEVERR_BLOCK_ID and that block reads as zeros.
+ *
+ * workspace: caller-owned device memory of workspace_bytes >=
+ * pa_decode_workspace_bytes(...). When workspace is NULL and one is needed,
+ * the library takes it with cudaMallocAsync on the stream and releases it with
+ * cudaFreeAsync after the merge. Too small a workspace returns PA_ERR_WORKSPACE.
+ *
+ * Supported: dtype f32/f16/bf16 (q, caches and out share it), head_dim 64 or
+ * 128, num_heads a multiple of num_kv_heads with num_heads/num_kv_heads <= 16,
+ * block_size a power of two in [1, 256].
+ */
+int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
+                              const void *value_cache, const int32_t *block_tables,
+                              int max_blocks_per_seq, const int32_t *context_lens,
+                              int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                              int block_size, int64_t num_blocks, float scale,
+                              int max_context_len, int partition_size, void *workspace,
+                              size_t workspace_bytes, int dtype, void *stream);
+
+/*
+ * Whole-block copies for copy-on-write.
+ * [P1 cow_write: a shared block is duplicated whole into a fresh block before
+ *  the write; P2 demo 3]
+ *
+ * For each pair (src, dst): key_cache[dst] = key_cache[src] and
+ * value_cache[dst] = value_cache[src] (all slots, heads and dims). Pairs with
+ * an id outside [0, num_blocks) are skipped and set PA_DEVERR_COPY_PAIR.
+ * Destinations must be distinct and must not appear as a source in the same
+ * call (caller error otherwise; pa_alloc_append never produces that).
+ */
+int pa_copy_blocks(void *key_cache, void *value_cache, const int32_t *src_dst_pairs,
+                   int64_t num_pairs, int64_t num_blocks, int block_size, int num_kv_heads,
+                   int head_dim, int dtype, void *stream);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's error word.
+ * *bits receives the PA_DEVERR_* bits seen since the last call. Returns
+ * PA_ERR_DEVICE_INDEX when any bit was set, PA_OK otherwise.
+ */
+int pa_get_device_error(void *stream, uint32_t *bits);
+
+/* ---- host block allocator ------------------------------------------------- */
+/*
+ * [P1 PagedKVManager: block pool whose free ids sit on a stack (initially
+ *  0..N-1 pushed in order, allocation pops the top), reference counts,
+ *  cow_write, free_sequence; P2 demo 1 (a new block only when a token starts
+ *  one), demo 3 (forked samples share blocks; copy-on-write on a shared
+ *  partial block)]
+ * Host memory only; no CUDA calls. Not thread-safe: one caller at a time per
+ * allocator object.
+ */
+typedef struct pa_allocator pa_allocator;
+
+typedef struct pa_alloc_stats {
+    int64_t num_blocks;
+    int64_t num_free;
+    int64_t num_used;
+    int64_t peak_used;
+    int64_t num_cow_copies;
+    int64_t num_seqs;
+} pa_alloc_stats;
+
+/* Create a pool of num_blocks blocks of block_size tokens. */
+int pa_alloc_create(int64_t num_blocks, int block_size, pa_allocator **out);
+void pa_alloc_destroy(pa_allocator *a);
+
+/* Register an empty sequence (PA_ERR_EXISTS if present). */
+int pa_alloc_add_seq(pa_allocator *a, int64_t seq_id);
+
+/* child shares every block of parent (each reference count + 1). */
+int pa_alloc_fork(pa_allocator *a, int64_t parent, int64_t child);
+
+/*
+ * Append n_tokens positions to seq_id. slots_out[n_tokens] receives each new
+ * position's slot. A position that starts a block takes a fresh block; a
+ * position inside a block whose reference count is above 1 first copies it
+ * (the (src, dst) pair is appended to cow_pairs_out, 2 ints per pair, at most
+ * cow_cap pairs) and the table is repointed. *n_cow receives the pair count.
+ * All-or-nothing: PA_ERR_OUT_OF_BLOCKS (or PA_ERR_INVALID_ARG when cow_cap is
+ * too small) leaves the allocator unchanged.
+ */
+int pa_alloc_append(pa_allocator *a, int64_t seq_id, int64_t n_tokens, int32_t *slots_out,
+                    int32_t *cow_pairs_out, int64_t cow_cap, int64_t *n_cow);
+
+/* Drop the sequence; blocks whose count reaches 0 return to the free stack. */
+int pa_alloc_free_seq(pa_allocator *a, int64_t seq_id);
+
+/* Copy seq_id's table into out[cap]; *n receives its length (may exceed cap). */
+int pa_alloc_block_table(const pa_allocator *a, int64_t seq_id, int32_t *out, int64_t cap,
+                         int64_t *n);
+
+/* Current length (tokens) of seq_id. */
+int pa_alloc_seq_len(const pa_allocator *a, int64_t seq_id, int64_t *len);
+
+/*
+ * Export a decode batch: row i of tables[n_seqs, max_blocks_per_seq] gets
+ * seq_ids[i]'s table padded with -1, context_lens[i] its length.
+ * PA_ERR_INVALID_ARG when a table is longer than max_blocks_per_seq.
+ */
+int pa_alloc_export(const pa_allocator *a, const int64_t *seq_ids, int64_t n_seqs,
+                    int32_t *tables, int max_blocks_per_seq, int32_t *context_lens);
+
+/* Raw pool operations (take one block with count 1; drop one reference). */
+int pa_alloc_block(pa_allocator *a, int32_t *block_out);
+int pa_alloc_decref(pa_allocator *a, int32_t block);
+
+/* Reference count of one block. */
+int pa_alloc_refcount(const pa_allocator *a, int32_t block, int32_t *count);
+
+int pa_alloc_get_stats(const pa_allocator *a, pa_alloc_stats *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

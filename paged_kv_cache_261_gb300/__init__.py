@@ -1,0 +1,249 @@
+"""Paged KV cache decode path for GB300 (sm_103a): Python binding of libpagedattn.
+
+A thin ctypes layer over the C ABI in ``include/pagedattn.h``: it reads shapes,
+dtypes and pointers off torch tensors and calls the library. Every step of the
+computation runs in the library's CUDA kernels; there is no fallback. Importing
+this package fails when ``_build/libpagedattn.so`` has not been built (run
+``python -m paged_kv_cache_261_gb300.build``).
+
+Entry points (same names as the C ABI, without the ``pa_`` prefix):
+  paged_kv_write(k, v, slot_mapping, key_cache, value_cache)
+  paged_attention_decode(out, q, key_cache, value_cache, block_tables,
+                         context_lens, scale, block_size, num_kv_heads)
+  copy_blocks(key_cache, value_cache, src_dst_pairs)
+  get_device_error()
+  BlockAllocator: the host block manager (free list, reference counts, fork,
+  copy-on-write, block-table and slot-mapping export).
+Cache layout: [num_blocks, block_size, num_kv_heads, head_dim].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpagedattn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libpagedattn.so is missing at {LIB_PATH}; build it with "
+        "`python -m paged_kv_cache_261_gb300.build` (needs nvcc)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = -1
+PA_ERR_UNSUPPORTED = -2
+PA_ERR_OUT_OF_BLOCKS = -3
+PA_ERR_CUDA = -4
+PA_ERR_DEVICE_INDEX = -5
+PA_ERR_UNKNOWN_SEQ = -6
+PA_ERR_WORKSPACE = -7
+PA_ERR_EXISTS = -8
+
+PA_DTYPE_F32, PA_DTYPE_F16, PA_DTYPE_BF16 = 0, 1, 2
+
+PA_DEVERR_SLOT = 0x1
+PA_DEVERR_BLOCK_ID = 0x2
+PA_DEVERR_CONTEXT = 0x4
+PA_DEVERR_COPY_PAIR = 0x8
+PA_DEVERR_WAIT = 0x10
+
+_vp, _i32, _i64, _sz, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+
+
+def _decl(name, args, res=ctypes.c_int):
+    fn = getattr(_lib, name)
+    fn.argtypes = args
+    fn.restype = res
+    return fn
+
+
+_decl("pa_status_string", [_i32], ctypes.c_char_p)
+_decl("pa_version", [])
+_decl("pa_paged_kv_write", [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp])
+_decl("pa_decode_workspace_bytes", [_i32, _i32, _i32, _i32, _i32], _sz)
+_decl("pa_paged_attention_decode", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                    _i64, _f, _i32, _i32, _vp, _sz, _i32, _vp])
+_decl("pa_copy_blocks", [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp])
+_decl("pa_get_device_error", [_vp, ctypes.POINTER(ctypes.c_uint32)])
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def status_string(status: int) -> str:
+    return _lib.pa_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(_lib.pa_version())
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raw ABI access)."""
+    return _lib
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != PA_OK:
+        raise PagedAttnError(rc, what)
+
+
+# ---------------------------------------------------------------------------
+# torch glue
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    m = {torch.float32: PA_DTYPE_F32, torch.float16: PA_DTYPE_F16, torch.bfloat16: PA_DTYPE_BF16}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _stream_ptr(stream, device) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _cuda(t, name: str, dtype=None, device=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def paged_kv_write(k, v, slot_mapping, key_cache, value_cache, stream=None) -> None:
+    """Scatter k/v [T, Hk, D] into key_cache/value_cache [NB, bs, Hk, D] at slot_mapping[T]."""
+    torch = _torch()
+    dev = key_cache.device
+    _cuda(key_cache, "key_cache")
+    _cuda(value_cache, "value_cache", key_cache.dtype, dev)
+    _cuda(k, "k", key_cache.dtype, dev)
+    _cuda(v, "v", key_cache.dtype, dev)
+    _cuda(slot_mapping, "slot_mapping", torch.int32, dev)
+    nb, bs, hk, d = key_cache.shape
+    if value_cache.shape != key_cache.shape:
+        raise ValueError("value_cache shape differs from key_cache")
+    T = slot_mapping.shape[0]
+    if tuple(k.shape) != (T, hk, d) or tuple(v.shape) != (T, hk, d):
+        raise ValueError(f"k/v must be [{T}, {hk}, {d}]")
+    rc = _lib.pa_paged_kv_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                                key_cache.data_ptr(), value_cache.data_ptr(), nb, bs, hk, d,
+                                _dtype_code(key_cache), _stream_ptr(stream, dev))
+    _check(rc, "pa_paged_kv_write")
+
+
+def decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                           partition_size: int = 0) -> int:
+    return int(_lib.pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len,
+                                              partition_size))
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(device, stream_ptr: int, nbytes: int):
+    """Cached per (device, stream) workspace buffer, grown on demand."""
+    torch = _torch()
+    key = (device, stream_ptr)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def paged_attention_decode(out, q, key_cache, value_cache, block_tables, context_lens, scale: float,
+                           block_size: int | None = None, num_kv_heads: int | None = None,
+                           max_context_len: int = 0, partition_size: int = 0, workspace=None,
+                           stream=None) -> None:
+    """out[b, h] = softmax(scale * q[b, h] . K_b^T) V_b over the paged cache.
+
+    q, out [B, H, D]; caches [NB, bs, Hk, D]; block_tables int32 [B, MB];
+    context_lens int32 [B]. max_context_len: host upper bound on the lengths
+    (0 = MB * bs). workspace: optional uint8 CUDA tensor; by default a cached
+    per-stream buffer is used."""
+    torch = _torch()
+    dev = key_cache.device
+    _cuda(key_cache, "key_cache")
+    _cuda(value_cache, "value_cache", key_cache.dtype, dev)
+    _cuda(q, "q", key_cache.dtype, dev)
+    _cuda(out, "out", key_cache.dtype, dev)
+    _cuda(block_tables, "block_tables", torch.int32, dev)
+    _cuda(context_lens, "context_lens", torch.int32, dev)
+    nb, bs, hk, d = key_cache.shape
+    if block_size is not None and block_size != bs:
+        raise ValueError(f"block_size {block_size} != cache block size {bs}")
+    if num_kv_heads is not None and num_kv_heads != hk:
+        raise ValueError(f"num_kv_heads {num_kv_heads} != cache kv heads {hk}")
+    if value_cache.shape != key_cache.shape:
+        raise ValueError("value_cache shape differs from key_cache")
+    B, H, D = q.shape
+    if D != d or tuple(out.shape) != (B, H, D):
+        raise ValueError("q/out must be [B, H, head_dim]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_tables must be [B, MB] and context_lens [B]")
+    mb = block_tables.shape[1]
+    sp = _stream_ptr(stream, dev)
+    need = decode_workspace_bytes(B, H, D, max_context_len or mb * bs, partition_size)
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            workspace = _workspace(dev, sp, need)
+        _cuda(workspace, "workspace", torch.uint8, dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    rc = _lib.pa_paged_attention_decode(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
+                                        value_cache.data_ptr(), block_tables.data_ptr(), mb,
+                                        context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
+                                        int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
+                                        _dtype_code(key_cache), sp)
+    _check(rc, "pa_paged_attention_decode")
+
+
+def copy_blocks(key_cache, value_cache, src_dst_pairs, stream=None) -> None:
+    """key_cache[dst] = key_cache[src] (and V) for each row (src, dst) of src_dst_pairs [P, 2]."""
+    torch = _torch()
+    dev = key_cache.device
+    _cuda(key_cache, "key_cache")
+    _cuda(value_cache, "value_cache", key_cache.dtype, dev)
+    _cuda(src_dst_pairs, "src_dst_pairs", torch.int32, dev)
+    if src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be [P, 2]")
+    nb, bs, hk, d = key_cache.shape
+    rc = _lib.pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr(), src_dst_pairs.data_ptr(),
+                             src_dst_pairs.shape[0], nb, bs, hk, d, _dtype_code(key_cache),
+                             _stream_ptr(stream, dev))
+    _check(rc, "pa_copy_blocks")
+
+
+def get_device_error(stream=None, device=None) -> int:
+    """Synchronise the stream; return and clear the PA_DEVERR_* bits of the device."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    bits = ctypes.c_uint32(0)
+    rc = _lib.pa_get_device_error(_stream_ptr(stream, dev), ctypes.byref(bits))
+    if rc not in (PA_OK, PA_ERR_DEVICE_INDEX):
+        raise PagedAttnError(rc, "pa_get_device_error")
+    return int(bits.value)
+
+
+from .allocator import AllocStats, BlockAllocator  # noqa: E402,F401

@@ -1,0 +1,230 @@
+// C-ABI entry points of libpagedattn: host-side validation, kernel selection,
+// split-K workspace handling and the device error word. The declarations and
+// their contracts are in include/pagedattn.h.
+#include <stdint.h>
+
+#include "../../include/pagedattn.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+// Per-device error word. Kernels receive its address as an argument.
+__device__ unsigned int g_device_error;
+
+unsigned int *g_err_ptr[pa::kMaxDevices] = {};
+
+int error_word(unsigned int **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= pa::kMaxDevices) return PA_ERR_CUDA;
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return PA_ERR_CUDA;
+        g_err_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    *out = g_err_ptr[dev];
+    return PA_OK;
+}
+
+int elem_size(int dtype) {
+    switch (dtype) {
+    case PA_DTYPE_F32: return 4;
+    case PA_DTYPE_F16: return 2;
+    case PA_DTYPE_BF16: return 2;
+    default: return 0;
+    }
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int ilog2(int64_t x) {
+    int r = 0;
+    while ((int64_t(1) << r) < x) ++r;
+    return r;
+}
+
+constexpr int kDefaultPartition = 512;
+
+int resolve_partition(int partition_size) { return partition_size == 0 ? kDefaultPartition : partition_size; }
+
+int64_t num_partitions(int64_t max_ctx, int part) {
+    if (max_ctx <= 0) return 1;
+    return (max_ctx + part - 1) / part;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t workspace_bytes_for(int64_t B, int64_t H, int64_t D, int64_t P) {
+    if (P <= 1) return 0;
+    return align256((size_t)(B * H * P * 2 * 4)) + (size_t)(B * H * P * D * 4);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(int status) {
+    switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_OUT_OF_BLOCKS: return "PA_ERR_OUT_OF_BLOCKS";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_DEVICE_INDEX: return "PA_ERR_DEVICE_INDEX";
+    case PA_ERR_UNKNOWN_SEQ: return "PA_ERR_UNKNOWN_SEQ";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_EXISTS: return "PA_ERR_EXISTS";
+    default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+int pa_version(void) { return 100; }
+
+int pa_paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping, int64_t num_tokens,
+                      void *key_cache, void *value_cache, int64_t num_blocks, int block_size,
+                      int num_kv_heads, int head_dim, int dtype, void *stream) {
+    const int es = elem_size(dtype);
+    if (es == 0 || num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * es;
+    if (row_bytes % 16 != 0 || row_bytes > (int64_t)1 << 30) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !key_cache || !value_cache) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    if (num_blocks > INT64_MAX / block_size) return PA_ERR_INVALID_ARG;
+    if ((num_tokens + 7) / 8 > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    unsigned int *err = nullptr;
+    if (int rc = error_word(&err)) return rc;
+    if (pa::launch_kv_write(k, v, slot_mapping, num_tokens, key_cache, value_cache,
+                            num_blocks * block_size, (int)row_bytes, err,
+                            static_cast<cudaStream_t>(stream)) != 0)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                 int partition_size) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size < 0)
+        return 0;
+    const int part = resolve_partition(partition_size);
+    return workspace_bytes_for(num_seqs, num_heads, head_dim, num_partitions(max_context_len, part));
+}
+
+int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
+                              const void *value_cache, const int32_t *block_tables,
+                              int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                              int num_heads, int num_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, float scale, int max_context_len,
+                              int partition_size, void *workspace, size_t workspace_bytes,
+                              int dtype, void *stream) {
+    if (elem_size(dtype) == 0 || num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+        max_blocks_per_seq <= 0 || max_context_len < 0 || partition_size < 0)
+        return PA_ERR_INVALID_ARG;
+    if (!pow2(block_size) || block_size > 256) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
+    if (partition_size != 0 && partition_size % 128 != 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+
+    const int64_t table_cap = (int64_t)max_blocks_per_seq * block_size;
+    const int64_t max_ctx = max_context_len == 0 ? table_cap : max_context_len;
+    if (max_ctx > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    const int part = resolve_partition(partition_size);
+    const int64_t P = num_partitions(max_ctx, part);
+    if (P > INT32_MAX / part) return PA_ERR_UNSUPPORTED;
+    int64_t limit = P * part < table_cap ? P * part : table_cap;
+    if (limit > max_ctx) limit = max_ctx;
+
+    pa::DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.key_cache = key_cache;
+    p.value_cache = value_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.num_blocks = num_blocks;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_heads / num_kv_heads;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.log2_block_size = ilog2(block_size);
+    p.partition_size = part;
+    p.max_partitions = (int)P;
+    p.context_limit = (int)limit;
+    p.scale_log2 = scale * pa::kLog2e;
+    if (int rc = error_word(&p.err)) return rc;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, P);
+    void *ws = workspace;
+    bool owned = false;
+    if (need > 0) {
+        if (ws) {
+            if (workspace_bytes < need) return PA_ERR_WORKSPACE;
+            if (!aligned16(ws)) return PA_ERR_INVALID_ARG;
+        } else {
+            if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return PA_ERR_CUDA;
+            owned = true;
+        }
+        p.ws_ml = static_cast<float *>(ws);
+        p.ws_o = reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                           align256((size_t)num_seqs * num_heads * P * 2 * 4));
+    }
+
+    int rc = pa::launch_decode_simt(p, dtype, s);
+    if (rc == 0 && P > 1) rc = pa::launch_decode_reduce(p, dtype, s);
+    if (owned) cudaFreeAsync(ws, s);
+    if (rc == -2) return PA_ERR_UNSUPPORTED;
+    return rc == 0 ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_copy_blocks(void *key_cache, void *value_cache, const int32_t *src_dst_pairs, int64_t num_pairs,
+                   int64_t num_blocks, int block_size, int num_kv_heads, int head_dim, int dtype,
+                   void *stream) {
+    const int es = elem_size(dtype);
+    if (es == 0 || num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes = (int64_t)block_size * num_kv_heads * head_dim * es;
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (num_pairs > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    if (!key_cache || !value_cache || !src_dst_pairs) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key_cache) || !aligned16(value_cache)) return PA_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    if (int rc = error_word(&err)) return rc;
+    if (pa::launch_copy_blocks(key_cache, value_cache, src_dst_pairs, num_pairs, num_blocks, block_bytes,
+                               err, static_cast<cudaStream_t>(stream)) != 0)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+int pa_get_device_error(void *stream, uint32_t *bits) {
+    if (!bits) return PA_ERR_INVALID_ARG;
+    *bits = 0;
+    unsigned int *err = nullptr;
+    if (int rc = error_word(&err)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int host = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaMemcpyAsync(&host, err, sizeof host, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaMemsetAsync(err, 0, sizeof host, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    *bits = host;
+    return host ? PA_ERR_DEVICE_INDEX : PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,362 @@
+// Decode attention, SIMT variant (fp32/fp16/bf16 caches; head_dim 64 or 128).
+//
+// Computes, for each sequence b and query head h (kv head h / G), the
+// single-query attention of "CS349E lecture 7: 01_paged_attention.py", demo 2,
+// paper eq. 4: scores against every cached key are formed block by block
+// through the block table, one softmax is taken over the whole context, and V
+// is accumulated block by block. The one softmax is computed online: a running
+// max and sum per head, rescaled whenever the max grows, give exactly the
+// softmax over the whole context once normalised.
+//
+// Work unit: one CTA per (partition of partition_size tokens, kv head,
+// sequence); all G query heads of the kv head share each K/V tile read. Tiles
+// of 32 tokens are gathered row by row through the block table with 16-byte
+// cp.async into a double-buffered shared-memory ring (rows XOR-swizzled at
+// 16-byte granularity so a warp reading 32 different rows is conflict-free).
+// Scores: lane = token, each warp owns whole query heads, so the tile max is a
+// warp shuffle reduction and no block barrier is needed for it. PV: each thread
+// owns two adjacent output columns of a subset of the heads.
+//
+// A sequence with one partition gets its final row here; otherwise the
+// partition writes its max (log2 units), sum and unnormalised output to the
+// workspace and decode_reduce merges them.
+#include <float.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pa {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kTile = 32;
+
+template <typename T, int D, int GT>
+struct SimtCfg {
+    static constexpr int kVN = Vec16<T>::N;                 // elements per 16-byte chunk
+    static constexpr int kChunks = D / kVN;                 // chunks per row
+    static constexpr int kRowBytes = D * (int)sizeof(T);
+    static constexpr int kHeadsPerWarp = (GT + 3) / 4;
+    static constexpr int kPairs = D / 2;
+    static constexpr int kHeadSlices = kThreads / kPairs;   // 2 (D=128) or 4 (D=64)
+    static constexpr int kHeadsPerThread = (GT + kHeadSlices - 1) / kHeadSlices;
+    // shared memory carve-up (bytes)
+    static constexpr int kQBytes = GT * D * 4;
+    static constexpr int kStageBytes = 2 * kTile * kRowBytes;   // K and V
+    static constexpr int kPBytes = kTile * GT * 4;
+    static constexpr int kSmem = kQBytes + 2 * kStageBytes + kPBytes + 4 * GT * 4;
+    static_assert(kChunks >= 8, "swizzle needs at least 8 chunks per row");
+};
+
+template <typename T, int D, int GT>
+__global__ __launch_bounds__(kThreads) void decode_simt_kernel(const DecodeParams p) {
+    using C = SimtCfg<T, D, GT>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float *q_s = reinterpret_cast<float *>(smem);                                   // [GT][D]
+    unsigned char *stage_base = smem + C::kQBytes;                                  // 2 stages
+    float *p_s = reinterpret_cast<float *>(smem + C::kQBytes + 2 * C::kStageBytes); // [kTile][GT]
+    float *alpha_s = p_s + kTile * GT;                                              // [GT]
+    float *m_s = alpha_s + GT;
+    float *l_s = m_s + GT;
+
+    const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = p.group;
+
+    int ctx = p.context_lens[b];
+    if (ctx < 0 || ctx > p.context_limit) {
+        if (tid == 0 && part == 0 && kvh == 0) raise_error(p.err, PA_DEVERR_CONTEXT);
+        ctx = ctx < 0 ? 0 : p.context_limit;
+    }
+    const int nparts = ctx == 0 ? 1 : (ctx + p.partition_size - 1) / p.partition_size;
+    if (part >= nparts) return;
+
+    T *out = reinterpret_cast<T *>(p.out);
+    const int64_t head0 = (int64_t)b * p.num_heads + (int64_t)kvh * G;
+    if (ctx == 0) {
+        for (int i = tid; i < G * D; i += kThreads) out[head0 * D + i] = Elem<T>::from_f(0.f);
+        return;
+    }
+    const int t0 = part * p.partition_size;
+    const int t1 = min(ctx, t0 + p.partition_size);
+
+    // queries of the group, pre-multiplied by scale*log2(e)
+    const T *q = reinterpret_cast<const T *>(p.q);
+    for (int i = tid; i < GT * D; i += kThreads) {
+        const int g = i / D;
+        q_s[i] = g < G ? Elem<T>::to_f(q[head0 * D + i]) * p.scale_log2 : 0.f;
+    }
+
+    const T *kc = reinterpret_cast<const T *>(p.key_cache);
+    const T *vc = reinterpret_cast<const T *>(p.value_cache);
+    const int32_t *table = p.block_tables + (int64_t)b * p.max_blocks_per_seq;
+    const int bs_mask = p.block_size - 1;
+
+    auto issue_tile = [&](int tile_start, int stage) {
+        unsigned char *ks = stage_base + stage * C::kStageBytes;
+        unsigned char *vs = ks + kTile * C::kRowBytes;
+        for (int idx = tid; idx < kTile * C::kChunks; idx += kThreads) {
+            const int r = idx / C::kChunks, c = idx % C::kChunks;
+            const int t = tile_start + r;
+            const T *ksrc = kc, *vsrc = vc;
+            int bytes = 0;
+            if (t < t1) {
+                const int32_t phys = table[t >> p.log2_block_size];
+                if (phys >= 0 && phys < p.num_blocks) {
+                    const int64_t row = ((int64_t)phys * p.block_size + (t & bs_mask)) * p.num_kv_heads + kvh;
+                    ksrc = kc + row * D + c * C::kVN;
+                    vsrc = vc + row * D + c * C::kVN;
+                    bytes = 16;
+                } else if (c == 0) {
+                    raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                }
+            }
+            const int off = r * C::kRowBytes + ((c ^ (r & 7)) * 16);
+            cp_async16(ks + off, ksrc, bytes);
+            cp_async16(vs + off, vsrc, bytes);
+        }
+    };
+
+    // per-warp running max (log2 units) of the heads the warp owns
+    float m_run[C::kHeadsPerWarp], l_lane[C::kHeadsPerWarp];
+#pragma unroll
+    for (int hh = 0; hh < C::kHeadsPerWarp; ++hh) {
+        m_run[hh] = -INFINITY;
+        l_lane[hh] = 0.f;
+    }
+    // PV accumulators: column pair `pair`, heads slice + kHeadSlices*k
+    const int pair = tid % C::kPairs, slice = tid / C::kPairs;
+    float o[C::kHeadsPerThread][2];
+#pragma unroll
+    for (int k = 0; k < C::kHeadsPerThread; ++k) o[k][0] = o[k][1] = 0.f;
+
+    const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+    issue_tile(t0, 0);
+    cp_async_commit();
+    for (int it = 0; it < ntiles; ++it) {
+        const int stage = it & 1;
+        if (it + 1 < ntiles) issue_tile(t0 + (it + 1) * kTile, stage ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+
+        const unsigned char *ks = stage_base + stage * C::kStageBytes;
+        const unsigned char *vs = ks + kTile * C::kRowBytes;
+        const int tile_start = t0 + it * kTile;
+        const int nvalid = min(kTile, t1 - tile_start);
+
+        // ---- scores: lane = token, warp owns heads warp, warp+4, ...
+        {
+            const int r = lane;
+            float acc[C::kHeadsPerWarp];
+#pragma unroll
+            for (int hh = 0; hh < C::kHeadsPerWarp; ++hh) acc[hh] = 0.f;
+#pragma unroll 4
+            for (int c = 0; c < C::kChunks; ++c) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(ks + r * C::kRowBytes + ((c ^ (r & 7)) * 16));
+                float kf[C::kVN];
+                Vec16<T>::unpack(raw, kf);
+#pragma unroll
+                for (int hh = 0; hh < C::kHeadsPerWarp; ++hh) {
+                    const int g = warp + 4 * hh;
+                    if (g < GT) {
+                        const float4 *qv = reinterpret_cast<const float4 *>(q_s + g * D + c * C::kVN);
+#pragma unroll
+                        for (int e4 = 0; e4 < C::kVN / 4; ++e4) {
+                            const float4 qq = qv[e4];
+                            acc[hh] = fmaf(qq.x, kf[4 * e4 + 0], acc[hh]);
+                            acc[hh] = fmaf(qq.y, kf[4 * e4 + 1], acc[hh]);
+                            acc[hh] = fmaf(qq.z, kf[4 * e4 + 2], acc[hh]);
+                            acc[hh] = fmaf(qq.w, kf[4 * e4 + 3], acc[hh]);
+                        }
+                    }
+                }
+            }
+            // ---- online softmax over the tile (warp-local per head)
+#pragma unroll
+            for (int hh = 0; hh < C::kHeadsPerWarp; ++hh) {
+                const int g = warp + 4 * hh;
+                if (g < GT) {
+                    const float s = r < nvalid ? acc[hh] : -INFINITY;
+                    float mx = s;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    const float m_new = fmaxf(m_run[hh], mx);
+                    const float alpha = fast_exp2(m_run[hh] - m_new);
+                    const float pr = r < nvalid ? fast_exp2(s - m_new) : 0.f;
+                    l_lane[hh] = l_lane[hh] * alpha + pr;
+                    m_run[hh] = m_new;
+                    p_s[r * GT + g] = pr;
+                    if (lane == 0) alpha_s[g] = alpha;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- PV: o[g][d] = o[g][d]*alpha[g] + sum_r p[r][g] * V[r][d]
+#pragma unroll
+        for (int k = 0; k < C::kHeadsPerThread; ++k) {
+            const int g = slice + C::kHeadSlices * k;
+            if (g < GT) {
+                const float a = alpha_s[g];
+                o[k][0] *= a;
+                o[k][1] *= a;
+            }
+        }
+        {
+            const int byte_in_row = pair * 2 * (int)sizeof(T);
+            const int c = byte_in_row / 16, within = byte_in_row % 16;
+            for (int r = 0; r < nvalid; ++r) {
+                const unsigned char *vp = vs + r * C::kRowBytes + ((c ^ (r & 7)) * 16) + within;
+                float v0, v1;
+                if constexpr (sizeof(T) == 4) {
+                    const float2 f = *reinterpret_cast<const float2 *>(vp);
+                    v0 = f.x; v1 = f.y;
+                } else {
+                    const T *e = reinterpret_cast<const T *>(vp);
+                    v0 = Elem<T>::to_f(e[0]);
+                    v1 = Elem<T>::to_f(e[1]);
+                }
+#pragma unroll
+                for (int k = 0; k < C::kHeadsPerThread; ++k) {
+                    const int g = slice + C::kHeadSlices * k;
+                    if (g < GT) {
+                        const float pr = p_s[r * GT + g];
+                        o[k][0] = fmaf(pr, v0, o[k][0]);
+                        o[k][1] = fmaf(pr, v1, o[k][1]);
+                    }
+                }
+            }
+        }
+        __syncthreads();   // stage `stage` and p_s are reused next iteration
+    }
+    cp_async_wait<0>();
+
+    // ---- per-head totals
+#pragma unroll
+    for (int hh = 0; hh < C::kHeadsPerWarp; ++hh) {
+        const int g = warp + 4 * hh;
+        if (g < GT) {
+            float l = l_lane[hh];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (lane == 0) {
+                m_s[g] = m_run[hh];
+                l_s[g] = l;
+            }
+        }
+    }
+    __syncthreads();
+
+    if (nparts == 1) {
+#pragma unroll
+        for (int k = 0; k < C::kHeadsPerThread; ++k) {
+            const int g = slice + C::kHeadSlices * k;
+            if (g < G) {
+                const float inv = 1.f / l_s[g];
+                T *dst = out + (head0 + g) * D + 2 * pair;
+                dst[0] = Elem<T>::from_f(o[k][0] * inv);
+                dst[1] = Elem<T>::from_f(o[k][1] * inv);
+            }
+        }
+    } else {
+        const int P = p.max_partitions;
+#pragma unroll
+        for (int k = 0; k < C::kHeadsPerThread; ++k) {
+            const int g = slice + C::kHeadSlices * k;
+            if (g < G) {
+                const int64_t row = (head0 + g) * P + part;
+                float2 *dst = reinterpret_cast<float2 *>(p.ws_o + row * D + 2 * pair);
+                *dst = make_float2(o[k][0], o[k][1]);
+                if (pair == 0) {
+                    p.ws_ml[2 * row] = m_s[g];
+                    p.ws_ml[2 * row + 1] = l_s[g];
+                }
+            }
+        }
+    }
+}
+
+// Merge of partition partials: M = max m_p, L = sum l_p 2^(m_p - M),
+// out = sum o_p 2^(m_p - M) / L. One CTA per (query head, sequence).
+template <typename T>
+__global__ __launch_bounds__(128) void decode_reduce_kernel(const DecodeParams p) {
+    const int h = blockIdx.x, b = blockIdx.y;
+    int ctx = p.context_lens[b];
+    if (ctx < 0 || ctx > p.context_limit) ctx = ctx < 0 ? 0 : p.context_limit;
+    const int nparts = ctx == 0 ? 1 : (ctx + p.partition_size - 1) / p.partition_size;
+    if (nparts <= 1) return;
+    const int D = p.head_dim, P = p.max_partitions;
+    const int64_t row0 = ((int64_t)b * p.num_heads + h) * P;
+    float M = -INFINITY;
+    for (int i = 0; i < nparts; ++i) M = fmaxf(M, p.ws_ml[2 * (row0 + i)]);
+    float L = 0.f;
+    for (int i = 0; i < nparts; ++i) L += p.ws_ml[2 * (row0 + i) + 1] * fast_exp2(p.ws_ml[2 * (row0 + i)] - M);
+    const float inv = 1.f / L;
+    T *out = reinterpret_cast<T *>(p.out) + ((int64_t)b * p.num_heads + h) * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float acc = 0.f;
+        for (int i = 0; i < nparts; ++i)
+            acc = fmaf(p.ws_o[(row0 + i) * D + d], fast_exp2(p.ws_ml[2 * (row0 + i)] - M), acc);
+        out[d] = Elem<T>::from_f(acc * inv);
+    }
+}
+
+template <typename T, int D, int GT>
+int launch_simt_t(const DecodeParams &p, cudaStream_t stream) {
+    using C = SimtCfg<T, D, GT>;
+    auto kern = decode_simt_kernel<T, D, GT>;
+    static bool attr_set[kMaxDevices] = {};   // the opt-in is per device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+            return -1;
+        attr_set[dev] = true;
+    }
+    dim3 grid((unsigned)p.max_partitions, (unsigned)p.num_kv_heads, (unsigned)p.num_seqs);
+    kern<<<grid, kThreads, C::kSmem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+template <typename T, int D>
+int launch_simt_g(const DecodeParams &p, cudaStream_t stream) {
+    const int G = p.group;
+    if (G <= 1) return launch_simt_t<T, D, 1>(p, stream);
+    if (G <= 2) return launch_simt_t<T, D, 2>(p, stream);
+    if (G <= 4) return launch_simt_t<T, D, 4>(p, stream);
+    if (G <= 8) return launch_simt_t<T, D, 8>(p, stream);
+    if (G <= 16) return launch_simt_t<T, D, 16>(p, stream);
+    return -2;
+}
+
+template <typename T>
+int launch_simt_d(const DecodeParams &p, cudaStream_t stream) {
+    if (p.head_dim == 64) return launch_simt_g<T, 64>(p, stream);
+    if (p.head_dim == 128) return launch_simt_g<T, 128>(p, stream);
+    return -2;
+}
+
+}  // namespace
+
+int launch_decode_simt(const DecodeParams &p, int dtype, cudaStream_t stream) {
+    switch (dtype) {
+    case PA_DTYPE_F32: return launch_simt_d<float>(p, stream);
+    case PA_DTYPE_F16: return launch_simt_d<__half>(p, stream);
+    case PA_DTYPE_BF16: return launch_simt_d<__nv_bfloat16>(p, stream);
+    default: return -2;
+    }
+}
+
+int launch_decode_reduce(const DecodeParams &p, int dtype, cudaStream_t stream) {
+    dim3 grid((unsigned)p.num_heads, (unsigned)p.num_seqs);
+    switch (dtype) {
+    case PA_DTYPE_F32: decode_reduce_kernel<float><<<grid, 128, 0, stream>>>(p); break;
+    case PA_DTYPE_F16: decode_reduce_kernel<__half><<<grid, 128, 0, stream>>>(p); break;
+    case PA_DTYPE_BF16: decode_reduce_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(p); break;
+    default: return -2;
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace pa

@@ -1,0 +1,52 @@
+// Internal launch interface between the C-ABI layer (capi.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Everything a decode kernel needs; built and validated by the C-ABI layer.
+struct DecodeParams {
+    void *out;
+    const void *q;
+    const void *key_cache;
+    const void *value_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    float *ws_ml;              // [B][H][P][2] running max (log2 units) and sum
+    float *ws_o;               // [B][H][P][D] unnormalised partial outputs
+    unsigned int *err;         // device error word
+    int64_t num_blocks;
+    int max_blocks_per_seq;
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int group;                 // num_heads / num_kv_heads
+    int head_dim;
+    int block_size;
+    int log2_block_size;
+    int partition_size;        // tokens per partition (multiple of 128)
+    int max_partitions;        // P: partitions per sequence the grid covers
+    int context_limit;         // min(max_blocks_per_seq*bs, P*partition_size)
+    float scale_log2;          // scale * log2(e)
+};
+
+int launch_kv_write(const void *k, const void *v, const int32_t *slot_mapping, int64_t num_tokens,
+                    void *key_cache, void *value_cache, int64_t num_slots, int row_bytes,
+                    unsigned int *err, cudaStream_t stream);
+
+int launch_copy_blocks(void *key_cache, void *value_cache, const int32_t *pairs, int64_t num_pairs,
+                       int64_t num_blocks, int64_t block_bytes, unsigned int *err,
+                       cudaStream_t stream);
+
+// SIMT partition kernel (any dtype); writes final rows for single-partition
+// sequences and partials for the rest.
+int launch_decode_simt(const DecodeParams &p, int dtype, cudaStream_t stream);
+
+// Merge of the partials of sequences with more than one partition.
+int launch_decode_reduce(const DecodeParams &p, int dtype, cudaStream_t stream);
+
+}  // namespace pa

@@ -291,7 +291,14 @@ class DecodeWorkload:
         return (self.kv_rows(TID_K, seq_idx, pos).reshape(shp),
                 self.kv_rows(TID_V, seq_idx, pos).reshape(shp))
 
-    def compact_host_view(self, seqs, rng_seed: int = 7, include_newest=False):
+    def _rows_host(self, seq_idx, pos):
+        """float32 numpy K and V rows, generated with torch's CPU threads."""
+        import torch
+        si = torch.from_numpy(np.ascontiguousarray(seq_idx))
+        pi = torch.from_numpy(np.ascontiguousarray(pos))
+        return (self.kv_rows(TID_K, si, pi).numpy(), self.kv_rows(TID_V, si, pi).numpy())
+
+    def compact_host_view(self, seqs, rng_seed: int = 7, include_newest=False, chunk: int = 16384):
         """A small host paged cache holding only ``seqs``.
 
         The chosen sequences' logical blocks are placed on a fresh random
@@ -313,13 +320,17 @@ class DecodeWorkload:
         nblk = max(total, 1)
         kc = np.zeros((nblk, bs, self.num_kv_heads, self.head_dim), np.float32)
         vc = np.zeros_like(kc)
+        kflat = kc.reshape(-1, self.row_elems)
+        vflat = vc.reshape(-1, self.row_elems)
         for i, b in enumerate(seqs):
-            k, v = self.contiguous_kv(int(b), include_newest=include_newest)
-            n = k.shape[0]
-            p = np.arange(n)
-            phys = tables[i, p // bs].astype(np.int64)
-            kc.reshape(-1, self.num_kv_heads, self.head_dim)[phys * bs + p % bs] = k
-            vc.reshape(-1, self.num_kv_heads, self.head_dim)[phys * bs + p % bs] = v
+            c = int(ctx[i])
+            n = c if include_newest else max(c - 1, 0)
+            for s in range(0, n, chunk):
+                p = np.arange(s, min(n, s + chunk), dtype=np.int64)
+                slot = tables[i, p // bs].astype(np.int64) * bs + p % bs
+                k, v = self._rows_host(np.full(p.shape[0], int(b), np.int64), p)
+                kflat[slot] = k
+                vflat[slot] = v
         newest = np.full(seqs.shape[0], -1, np.int32)
         for i, c in enumerate(ctx):
             if c > 0:
