@@ -344,9 +344,9 @@ def run_ours(args):
         dist.init_process_group("nccl")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    from paged_kv_cache_261_gb300.build import build_library
+    from __graft_entry__ import build
     if rank == 0 or world == 1:
-        build_library()
+        build()
     if world > 1:
         dist.barrier()
 

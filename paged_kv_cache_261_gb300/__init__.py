@@ -4,7 +4,7 @@ A thin ctypes layer over the C ABI in ``include/pagedattn.h``: it reads shapes,
 dtypes and pointers off torch tensors and calls the library. Every step of the
 computation runs in the library's CUDA kernels; there is no fallback. Importing
 this package fails when ``_build/libpagedattn.so`` has not been built (run
-``python -m paged_kv_cache_261_gb300.build``).
+``python paged_kv_cache_261_gb300/build.py``).
 
 Entry points (same names as the C ABI, without the ``pa_`` prefix):
   paged_kv_write(k, v, slot_mapping, key_cache, value_cache)
@@ -29,7 +29,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libpagedattn.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"libpagedattn.so is missing at {LIB_PATH}; build it with "
-        "`python -m paged_kv_cache_261_gb300.build` (needs nvcc)")
+        "`python paged_kv_cache_261_gb300/build.py` (needs nvcc)")
 
 _lib = ctypes.CDLL(LIB_PATH)
 

@@ -12,8 +12,8 @@ TOL = {"f32": (1e-5, 1e-5), "f16": (2e-2, 2e-3), "bf16": (2e-2, 2e-3)}
 
 
 def pa_mod():
-    from paged_kv_cache_261_gb300.build import build_library
-    build_library()
+    from __graft_entry__ import build
+    build()
     import paged_kv_cache_261_gb300 as pa
     return pa
 

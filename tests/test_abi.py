@@ -13,8 +13,8 @@ from conftest import ROOT
 
 @pytest.fixture(scope="module")
 def pa():
-    from paged_kv_cache_261_gb300.build import build_library
-    build_library()
+    from __graft_entry__ import build
+    build()
     import paged_kv_cache_261_gb300 as pa
     return pa
 
