@@ -141,6 +141,39 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
                               size_t workspace_bytes, int dtype, void *stream);
 
 /*
+ * Decode attention that allocates no device memory. The paper has no
+ * counterpart to this entry point; it exists for callers, not for the method.
+ *
+ * Same computation, arguments and results as pa_paged_attention_decode, minus
+ * the workspace. It is meant for callers that can neither allocate device
+ * memory nor lend a buffer: for example a process whose device memory belongs to
+ * a host runtime that forbids libraries to allocate, or a serving loop that
+ * cannot afford an allocation on its critical path. The split-K scratch comes
+ * from a fixed array of PA_NOALLOC_SCRATCH_BYTES inside this library, which every
+ * GPU that loads the library holds until the process exits; no call allocates
+ * or frees anything.
+ *
+ * Limit: when pa_decode_workspace_bytes(num_seqs, num_heads, head_dim,
+ * max_context_len or max_blocks_per_seq*block_size, partition_size) exceeds
+ * PA_NOALLOC_SCRATCH_BYTES the call returns PA_ERR_WORKSPACE and launches nothing.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture. All calls on
+ * a device share the array and it keeps the previous call's contents (nothing
+ * in it needs to start at zero). Calls that overlap on the GPU race on it:
+ * order them (one stream, or events between streams).
+ */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+int pa_paged_attention_decode_noalloc(void *out, const void *q, const void *key_cache,
+                                      const void *value_cache, const int32_t *block_tables,
+                                      int max_blocks_per_seq, const int32_t *context_lens,
+                                      int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int64_t num_blocks, float scale,
+                                      int max_context_len, int partition_size, int dtype,
+                                      void *stream);
+
+/*
  * Whole-block copies for copy-on-write.
  * [P1 cow_write: a shared block is duplicated whole into a fresh block before
  *  the write; P2 demo 3]
