@@ -235,6 +235,7 @@ class Step:
                 "written_tokens": int(self.slots.shape[0]),
                 "copied_blocks": 0 if self.copy_pairs is None else int(self.copy_pairs.shape[0]),
                 "partition_size": 512,
+                "decode_kernel": os.environ.get("PA_DECODE_KERNEL", "auto"),
                 "l2": f"inputs larger than L2: {w.algorithmic_bytes()['kv'] / 1e9:.2f} GB of K/V read per step "
                       f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"}
 

@@ -2,6 +2,8 @@
 // split-K workspace handling and the device error word. The declarations and
 // their contracts are in include/pagedattn.h.
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "../../include/pagedattn.h"
 #include "common.cuh"
@@ -51,6 +53,17 @@ int resolve_partition(int partition_size) { return partition_size == 0 ? kDefaul
 int64_t num_partitions(int64_t max_ctx, int part) {
     if (max_ctx <= 0) return 1;
     return (max_ctx + part - 1) / part;
+}
+
+// Decode kernel choice: the tensor-core kernel where it applies, else SIMT.
+// PA_DECODE_KERNEL=simt or =tc in the environment forces one (tests compare both).
+enum class DecodeKernel { Auto, Simt, Tc };
+DecodeKernel decode_kernel_choice() {
+    const char *e = getenv("PA_DECODE_KERNEL");
+    if (!e) return DecodeKernel::Auto;
+    if (!strcmp(e, "simt")) return DecodeKernel::Simt;
+    if (!strcmp(e, "tc")) return DecodeKernel::Tc;
+    return DecodeKernel::Auto;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -184,7 +197,12 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
                                            align256((size_t)num_seqs * num_heads * P * 2 * 4));
     }
 
-    int rc = pa::launch_decode_simt(p, dtype, s);
+    const DecodeKernel choice = decode_kernel_choice();
+    int rc;
+    if (choice == DecodeKernel::Tc || (choice == DecodeKernel::Auto && pa::decode_tc_supported(p, dtype)))
+        rc = pa::launch_decode_tc(p, dtype, s);
+    else
+        rc = pa::launch_decode_simt(p, dtype, s);
     if (rc == 0 && P > 1) rc = pa::launch_decode_reduce(p, dtype, s);
     if (owned) cudaFreeAsync(ws, s);
     if (rc == -2) return PA_ERR_UNSUPPORTED;

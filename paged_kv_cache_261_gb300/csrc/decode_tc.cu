@@ -1,0 +1,604 @@
+// Decode attention on the sm_100 tensor cores (tcgen05) with TMA block gathers.
+//
+// Computes what "CS349E lecture 7: 01_paged_attention.py", demo 2, paper eq. 4
+// defines: for each sequence and query head, scores against every cached key
+// are formed block by block through the block table, one softmax is taken over
+// the whole context, and V is accumulated block by block. The softmax is taken
+// online (running max and sum per head, rescaled when the max grows), which
+// equals the softmax over the whole context once normalised; partitions of a
+// long context are merged by decode_reduce_kernel.
+//
+// Shape of the work. All G query heads of a kv head share one K/V read, so
+// per 128-token tile the contraction is S^T[128 tok x 16] = K[128 x 128] . Q^T
+// and O^T[128 d x 16] = V^T[128 x 128 tok] . P^T: two M=128, N=16 (G padded),
+// K=128 tcgen05 MMAs with bf16/f16 operands in shared memory and fp32
+// accumulators in tensor memory. The tensor cores take the G-fold reuse of each
+// K/V element off the FP32 pipes; the kernel stays bound by HBM.
+//
+// CTA = one persistent worker per SM; 192 threads in three roles:
+//   warp 0    TMA producer: per tile, reads the tile's table entries (one lane
+//             per physical block) and loads each block's K and V rows
+//             (box = 64 dims x block_size tokens of one kv head, 128-byte
+//             swizzle) plus the group's queries into a 3-stage ring. Blocks
+//             past the partition end or with a bad id load from an
+//             out-of-range coordinate, which TMA fills with zeros.
+//   warp 1    MMA issuer (one thread) and tensor-memory owner: S for tile i
+//             into a double-buffered S accumulator, then O for tile i-1 once
+//             its probabilities are in shared memory.
+//   warps 2-5 softmax and output (thread = token for S, thread = dim for O):
+//             scale, mask, tile max through shuffles + shared memory, exp2,
+//             P^T to shared memory (bf16/f16, 128-byte swizzled K-major), zero
+//             V rows of masked tokens (their contents may be anything), and
+//             o = o * alpha + O_tile in registers.
+// Work items = (sequence, partition, kv head), enumerated from a prefix sum of
+// partitions per sequence built in shared memory at kernel start, assigned to
+// CTAs round-robin. Every wait is bounded (see sm100.cuh); on a timeout the
+// kernel sets PA_DEVERR_WAIT, drains its copies and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace pa {
+namespace {
+
+using namespace sm100;
+
+constexpr int kD = 128;
+constexpr int kTile = 128;                        // tokens per MMA tile (M)
+constexpr int kN = 16;                            // MMA N: query heads of a group, padded
+constexpr int kStages = 3;
+constexpr int kChunkBytes = kTile * 128;          // 128 rows x 64 dims x 2 B
+constexpr int kKVBytes = 2 * kChunkBytes;         // one tile of K (or V), both 64-dim halves
+constexpr int kQBytes = 2 * kN * 128;             // 16 rows x 128 dims
+constexpr int kPBytes = 2 * kN * 128;             // P^T: 16 rows x 128 tokens
+constexpr int kTxBytes = 2 * kKVBytes + kQBytes;  // bytes TMA delivers per stage
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kMaxPrefixSeqs = 2048;
+constexpr uint32_t kTmemCols = 64;                // S[2] x 16 + O[2] x 16 columns
+
+// shared-memory carve-up (from a 1024-aligned base)
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kStages * kKVBytes;
+constexpr int kOffQ = kOffV + kStages * kKVBytes;
+constexpr int kOffP = kOffQ + kStages * kQBytes;
+constexpr int kOffRed = kOffP + 2 * kPBytes;                  // float [2][4][16]
+constexpr int kOffLRed = kOffRed + 2 * 4 * kN * 4;            // float [4][16]
+constexpr int kOffBar = kOffLRed + 4 * kN * 4;                // uint64 barriers
+constexpr int kNumBars = 4 * kStages + 12;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;              // tmem base, abort flag
+constexpr int kOffPrefix = kOffMisc + 16;                     // int [kMaxPrefixSeqs + 1]
+constexpr int kSmemUsed = kOffPrefix + (kMaxPrefixSeqs + 1) * 4;
+constexpr int kSmemBytes = kSmemUsed + 1024;                  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Bars {
+    uint64_t *full, *empty;        // [kStages]
+    uint64_t *s_full, *s_free;     // [2]
+    uint64_t *p_full, *o_full;     // [2]
+    uint64_t *o_free, *red;        // [2]
+    uint64_t *fin;                 // [1]
+};
+
+struct Item {
+    int b, kvh, part, nparts, t0, t1, ntiles;
+};
+
+__device__ __forceinline__ Item get_item(int idx, const int *prefix, const DecodeParams &p) {
+    Item it;
+    const int pair = idx / p.num_kv_heads;
+    it.kvh = idx - pair * p.num_kv_heads;
+    int lo = 0, hi = p.num_seqs;                  // prefix[lo] <= pair < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= pair) lo = mid; else hi = mid;
+    }
+    it.b = lo;
+    it.part = pair - prefix[lo];
+    it.nparts = prefix[lo + 1] - prefix[lo];
+    int ctx = p.context_lens[lo];
+    ctx = ctx < 0 ? 0 : (ctx > p.context_limit ? p.context_limit : ctx);
+    it.t0 = it.part * p.partition_size;
+    it.t1 = min(ctx, it.t0 + p.partition_size);
+    it.ntiles = it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
+    return it;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <typename T> __device__ __forceinline__ uint16_t to_bits(float x);
+template <> __device__ __forceinline__ uint16_t to_bits<__nv_bfloat16>(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <> __device__ __forceinline__ uint16_t to_bits<__half>(float x) {
+    return __half_as_ushort(__float2half_rn(x));
+}
+template <typename T> __device__ __forceinline__ float from_bits(uint16_t b);
+template <> __device__ __forceinline__ float from_bits<__nv_bfloat16>(uint16_t b) {
+    return __uint_as_float((uint32_t)b << 16);
+}
+template <> __device__ __forceinline__ float from_bits<__half>(uint16_t b) {
+    return __half2float(__ushort_as_half(b));
+}
+
+template <typename T, int GT>
+__global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                const __grid_constant__ CUtensorMap tm_v,
+                                                                const __grid_constant__ CUtensorMap tm_q,
+                                                                const DecodeParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *sK = smem + kOffK;
+    unsigned char *sV = smem + kOffV;
+    unsigned char *sQ = smem + kOffQ;
+    unsigned char *sP = smem + kOffP;
+    float *red = reinterpret_cast<float *>(smem + kOffRed);
+    float *lred = reinterpret_cast<float *>(smem + kOffLRed);
+    uint64_t *bar_base = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    int *prefix = reinterpret_cast<int *>(smem + kOffPrefix);
+
+    Bars bars;
+    bars.full = bar_base;
+    bars.empty = bar_base + kStages;
+    bars.s_full = bar_base + 2 * kStages;
+    bars.s_free = bars.s_full + 2;
+    bars.p_full = bars.s_free + 2;
+    bars.o_full = bars.p_full + 2;
+    bars.o_free = bars.o_full + 2;
+    bars.red = bars.o_free + 2;
+    bars.fin = bars.red + 2;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = p.group;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.s_free[i], 4);
+            mbar_init(&bars.p_full[i], 4);
+            mbar_init(&bars.o_full[i], 1);
+            mbar_init(&bars.o_free[i], 4);
+            mbar_init(&bars.red[i], kSoftmaxThreads);
+        }
+        mbar_init(bars.fin, kSoftmaxThreads);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    // partitions per sequence -> exclusive prefix sum in shared memory
+    const int B = p.num_seqs;
+    for (int b = tid; b < B; b += kThreads) {
+        int ctx = p.context_lens[b];
+        if (ctx < 0 || ctx > p.context_limit) {
+            if (blockIdx.x == 0) raise_error(p.err, PA_DEVERR_CONTEXT);
+            ctx = ctx < 0 ? 0 : p.context_limit;
+        }
+        prefix[b + 1] = ctx == 0 ? 1 : (ctx + p.partition_size - 1) / p.partition_size;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (B + 31) / 32;
+        const int lo = 1 + lane * per, hi = min(B + 1, lo + per);
+        int sum = 0;
+        for (int i = lo; i < hi; ++i) sum += prefix[i];
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        int run = incl - sum;
+        for (int i = lo; i < hi; ++i) {
+            run += prefix[i];
+            prefix[i] = run;
+        }
+        if (lane == 0) prefix[0] = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total_items = prefix[B] * p.num_kv_heads;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const int nbt = kTile / p.block_size;       // physical blocks per tile
+        uint32_t it = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+            const Item I = get_item(idx, prefix, p);
+            const int32_t *table = p.block_tables + (int64_t)I.b * p.max_blocks_per_seq;
+            const int qrow = I.b * p.num_heads + I.kvh * G;
+            for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
+                const int stage = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                const int tstart = I.t0 + tile * kTile;
+                int phys = (int)p.num_blocks;           // out of range: TMA fills zeros
+                if (lane < nbt) {
+                    const int tok = tstart + lane * p.block_size;
+                    if (tok < I.t1) {
+                        const int e = table[tok >> p.log2_block_size];
+                        if (e >= 0 && e < p.num_blocks) phys = e;
+                        else raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                    }
+                }
+                int w = 1;
+                if (lane == 0) w = mbar_wait(&bars.empty[stage], ph ^ 1) ? 1 : 0;
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&bars.full[stage], kTxBytes);
+                __syncwarp();
+                if (lane < nbt) {
+                    unsigned char *dk = sK + stage * kKVBytes + lane * p.block_size * 128;
+                    unsigned char *dv = sV + stage * kKVBytes + lane * p.block_size * 128;
+                    tma_load_4d(dk, &tm_k, &bars.full[stage], 0, I.kvh, 0, phys);
+                    tma_load_4d(dk + kChunkBytes, &tm_k, &bars.full[stage], 64, I.kvh, 0, phys);
+                    tma_load_4d(dv, &tm_v, &bars.full[stage], 0, I.kvh, 0, phys);
+                    tma_load_4d(dv + kChunkBytes, &tm_v, &bars.full[stage], 64, I.kvh, 0, phys);
+                }
+                if (lane == 0) {
+                    unsigned char *dq = sQ + stage * kQBytes;
+                    tma_load_2d(dq, &tm_q, &bars.full[stage], 0, qrow);
+                    tma_load_2d(dq + kN * 128, &tm_q, &bars.full[stage], 64, qrow);
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            raise_error(p.err, PA_DEVERR_WAIT);
+        }
+        // drain: every issued stage's copies must have landed before the CTA exits
+        if (lane == 0) {
+            const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
+            for (uint32_t j = first; j < it; ++j) mbar_wait(&bars.full[j % kStages], (j / kStages) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+            const uint32_t idesc_s = instr_desc_f16(kTile, kN, kBf16, false, false);
+            const uint32_t idesc_o = instr_desc_f16(kD, kN, kBf16, true, false);
+            const uint32_t sK0 = smem_addr(sK), sV0 = smem_addr(sV), sQ0 = smem_addr(sQ), sP0 = smem_addr(sP);
+            uint32_t it = 0;
+            bool ok = true;
+            bool have_prev = false;
+            uint32_t prev_it = 0;
+            auto issue_pv = [&](uint32_t j) -> bool {
+                const int buf = j & 1, stage = j % kStages;
+                const uint32_t bph = (j >> 1) & 1;
+                if (!mbar_wait(&bars.p_full[buf], bph)) return false;
+                if (!mbar_wait(&bars.o_free[buf], bph ^ 1)) return false;
+                tc_fence_after();
+                const uint32_t vbase = sV0 + stage * kKVBytes;
+                const uint32_t pbase = sP0 + buf * kPBytes;
+                const uint32_t dcol = tmem + 2 * kN + buf * kN;
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    const uint64_t a = smem_desc(vbase + kk * 2048, kChunkBytes, 1024);
+                    const uint64_t b = smem_desc(pbase + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+                    mma_f16(dcol, a, b, idesc_o, kk > 0);
+                }
+                mma_commit(&bars.o_full[buf]);
+                mma_commit(&bars.empty[stage]);
+                return true;
+            };
+            for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+                const Item I = get_item(idx, prefix, p);
+                for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
+                    const int stage = it % kStages, buf = it & 1;
+                    if (*abort_flag || !mbar_wait(&bars.full[stage], (it / kStages) & 1) ||
+                        !mbar_wait(&bars.s_free[buf], ((it >> 1) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kbase = sK0 + stage * kKVBytes;
+                    const uint32_t qbase = sQ0 + stage * kQBytes;
+                    const uint32_t dcol = tmem + buf * kN;
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                        const uint32_t qoff = (kk >> 2) * (kN * 128) + (kk & 3) * 32;
+                        const uint64_t a = smem_desc(kbase + off, 16, 1024);
+                        const uint64_t b = smem_desc(qbase + qoff, 16, 1024);
+                        mma_f16(dcol, a, b, idesc_s, kk > 0);
+                    }
+                    mma_commit(&bars.s_full[buf]);
+                    if (have_prev && !issue_pv(prev_it)) {
+                        ok = false;
+                        break;
+                    }
+                    have_prev = true;
+                    prev_it = it;
+                }
+            }
+            if (ok && have_prev && !issue_pv(prev_it)) ok = false;
+            if (!ok) {
+                *abort_flag = 1;
+                raise_error(p.err, PA_DEVERR_WAIT);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax / output
+        const int q4 = warp & 3;                       // tensor-memory lane quadrant
+        const int row = q4 * 32 + lane;                // token (S) or dim (O) of this thread
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        T *out = reinterpret_cast<T *>(p.out);
+        uint32_t it = 0, nfin = 0;              // tile counter; uses of the finalize barrier
+        bool ok = true;
+        float m_run[GT], l_part[GT], o_acc[GT], alpha_prev[GT];
+        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+            const Item I = get_item(idx, prefix, p);
+            const int64_t head0 = (int64_t)I.b * p.num_heads + (int64_t)I.kvh * G;
+            if (I.ntiles == 0) {
+#pragma unroll
+                for (int g = 0; g < GT; ++g)
+                    if (g < G) out[(head0 + g) * kD + row] = Elem<T>::from_f(0.f);
+                continue;
+            }
+#pragma unroll
+            for (int g = 0; g < GT; ++g) {
+                m_run[g] = -INFINITY;
+                l_part[g] = 0.f;
+                o_acc[g] = 0.f;
+                alpha_prev[g] = 0.f;
+            }
+            auto accumulate = [&](uint32_t j) -> bool {
+                const int buf = j & 1;
+                if (!mbar_wait(&bars.o_full[buf], (j >> 1) & 1)) return false;
+                tc_fence_after();
+                float o[16];
+                tmem_ld16(tmem + lane_off + 2 * kN + buf * kN, o);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.o_free[buf]);
+#pragma unroll
+                for (int g = 0; g < GT; ++g) o_acc[g] = fmaf(o_acc[g], alpha_prev[g], o[g]);
+                return true;
+            };
+            for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
+                const int buf = it & 1, stage = it % kStages;
+                if (*abort_flag || !mbar_wait(&bars.s_full[buf], (it >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float s[16];
+                tmem_ld16(tmem + lane_off + buf * kN, s);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.s_free[buf]);
+
+                const int tok = I.t0 + tile * kTile + row;
+                const bool valid = tok < I.t1;
+                float* rd = red + (it & 1) * 4 * kN;
+#pragma unroll
+                for (int g = 0; g < GT; ++g) {
+                    s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
+                    const float mx = warp_max(s[g]);
+                    if (lane == 0) rd[q4 * kN + g] = mx;
+                }
+                mbar_arrive(&bars.red[it & 1]);
+                if (!mbar_wait(&bars.red[it & 1], (it >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                float alpha[GT];
+                unsigned char *pb = sP + buf * kPBytes + (row >> 6) * (kN * 128);
+                const int colb = (row & 63) * 2;
+#pragma unroll
+                for (int g = 0; g < GT; ++g) {
+                    const float tmax = fmaxf(fmaxf(rd[g], rd[kN + g]), fmaxf(rd[2 * kN + g], rd[3 * kN + g]));
+                    const float m_new = fmaxf(m_run[g], tmax);
+                    alpha[g] = fast_exp2(m_run[g] - m_new);
+                    m_run[g] = m_new;
+                    const uint16_t bits = to_bits<T>(valid ? fast_exp2(s[g] - m_new) : 0.f);
+                    l_part[g] = fmaf(l_part[g], alpha[g], from_bits<T>(bits));
+                    // P^T element (row n = g, column k = token) in a 128-byte swizzled K-major tile
+                    unsigned char *dst = pb + g * 128 + ((((colb >> 4) ^ (g & 7)) << 4) | (colb & 15));
+                    *reinterpret_cast<uint16_t *>(dst) = bits;
+                }
+                if (!valid) {
+                    // masked token: its V row may hold anything (NaN included) and P = 0
+                    if (!mbar_wait(&bars.full[stage], (it / kStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    uint4 *v0 = reinterpret_cast<uint4 *>(sV + stage * kKVBytes + row * 128);
+                    uint4 *v1 = reinterpret_cast<uint4 *>(sV + stage * kKVBytes + kChunkBytes + row * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        v0[c] = make_uint4(0, 0, 0, 0);
+                        v1[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.p_full[buf]);
+                if (tile > 0 && !accumulate(it - 1)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int g = 0; g < GT; ++g) alpha_prev[g] = alpha[g];
+            }
+            if (!ok) break;
+            if (!accumulate(it - 1)) {
+                ok = false;
+                break;
+            }
+            // ---- finalize the item: sum of the token lanes' partial l per head
+#pragma unroll
+            for (int g = 0; g < GT; ++g) {
+                const float ls = warp_sum(l_part[g]);
+                if (lane == 0) lred[q4 * kN + g] = ls;
+            }
+            mbar_arrive(bars.fin);
+            if (!mbar_wait(bars.fin, nfin++ & 1)) {
+                ok = false;
+                break;
+            }
+            float l_tot[GT];
+#pragma unroll
+            for (int g = 0; g < GT; ++g) l_tot[g] = lred[g] + lred[kN + g] + lred[2 * kN + g] + lred[3 * kN + g];
+            mbar_arrive(bars.fin);                    // lred may be rewritten after this phase
+            if (!mbar_wait(bars.fin, nfin++ & 1)) {
+                ok = false;
+                break;
+            }
+            if (I.nparts == 1) {
+#pragma unroll
+                for (int g = 0; g < GT; ++g)
+                    if (g < G) out[(head0 + g) * kD + row] = Elem<T>::from_f(o_acc[g] / l_tot[g]);
+            } else {
+                const int P = p.max_partitions;
+#pragma unroll
+                for (int g = 0; g < GT; ++g) {
+                    if (g < G) {
+                        const int64_t r = (head0 + g) * P + I.part;
+                        p.ws_o[r * kD + row] = o_acc[g];
+                        if (row == 0) {
+                            p.ws_ml[2 * r] = m_run[g];
+                            p.ws_ml[2 * r + 1] = l_tot[g];
+                        }
+                    }
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            raise_error(p.err, PA_DEVERR_WAIT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---- host side -----------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool make_cache_map(CUtensorMap *m, const void *base, const DecodeParams &p, CUtensorMapDataType dt) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t es = 2;
+    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)p.num_kv_heads, (cuuint64_t)p.block_size,
+                          (cuuint64_t)p.num_blocks};
+    cuuint64_t strides[3] = {kD * es, (cuuint64_t)p.num_kv_heads * kD * es,
+                             (cuuint64_t)p.block_size * p.num_kv_heads * kD * es};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)p.block_size, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_q_map(CUtensorMap *m, const DecodeParams &p, CUtensorMapDataType dt) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.num_seqs * p.num_heads};
+    cuuint64_t strides[1] = {kD * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kN};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, dt, 2, const_cast<void *>(p.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int GT>
+int launch_tc_t(const DecodeParams &p, CUtensorMapDataType dt, cudaStream_t stream) {
+    auto kern = decode_tc_kernel<T, GT>;
+    static bool attr_set[kMaxDevices] = {};
+    static int num_sms[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+            return -1;
+        if (cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        attr_set[dev] = true;
+    }
+    CUtensorMap mk, mv, mq;
+    if (!make_cache_map(&mk, p.key_cache, p, dt) || !make_cache_map(&mv, p.value_cache, p, dt) ||
+        !make_q_map(&mq, p, dt))
+        return -1;
+    const int64_t max_items = (int64_t)p.num_seqs * p.num_kv_heads * p.max_partitions;
+    const int grid = (int)(max_items < num_sms[dev] ? max_items : num_sms[dev]);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, mq, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+template <typename T>
+int launch_tc_g(const DecodeParams &p, CUtensorMapDataType dt, cudaStream_t stream) {
+    if (p.group <= 4) return launch_tc_t<T, 4>(p, dt, stream);
+    if (p.group <= 8) return launch_tc_t<T, 8>(p, dt, stream);
+    return launch_tc_t<T, 16>(p, dt, stream);
+}
+
+}  // namespace
+
+bool decode_tc_supported(const DecodeParams &p, int dtype) {
+    return (dtype == PA_DTYPE_BF16 || dtype == PA_DTYPE_F16) && p.head_dim == kD && p.group >= 1 &&
+           p.group <= kN && p.block_size >= 8 && p.block_size <= kTile && p.partition_size % kTile == 0 &&
+           p.num_seqs <= kMaxPrefixSeqs && p.num_blocks < INT32_MAX &&
+           (int64_t)p.num_seqs * p.num_heads < INT32_MAX;
+}
+
+int launch_decode_tc(const DecodeParams &p, int dtype, cudaStream_t stream) {
+    if (!decode_tc_supported(p, dtype)) return -2;
+    if (dtype == PA_DTYPE_BF16) return launch_tc_g<__nv_bfloat16>(p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, stream);
+    return launch_tc_g<__half>(p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, stream);
+}
+
+}  // namespace pa

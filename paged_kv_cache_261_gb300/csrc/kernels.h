@@ -46,6 +46,11 @@ int launch_copy_blocks(void *key_cache, void *value_cache, const int32_t *pairs,
 // sequences and partials for the rest.
 int launch_decode_simt(const DecodeParams &p, int dtype, cudaStream_t stream);
 
+// Tensor-core partition kernel (bf16/f16, head_dim 128, group <= 16, block
+// size 8..128). decode_tc_supported tells whether it covers a call.
+bool decode_tc_supported(const DecodeParams &p, int dtype);
+int launch_decode_tc(const DecodeParams &p, int dtype, cudaStream_t stream);
+
 // Merge of the partials of sequences with more than one partition.
 int launch_decode_reduce(const DecodeParams &p, int dtype, cudaStream_t stream);
 

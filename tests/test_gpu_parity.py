@@ -362,3 +362,50 @@ def test_bad_copy_pair_sets_the_error(pa):
     pa.copy_blocks(kc, vc, torch.tensor([[0, 9], [1, 2]], dtype=torch.int32, device=d))
     assert pa.get_device_error() & pa.PA_DEVERR_COPY_PAIR
     assert torch.equal(kc[2], before[1]) and torch.equal(kc[0], before[0])
+
+
+# ---------------------------------------------------------------------------
+# both decode kernels (tensor-core and SIMT) against the oracle
+# ---------------------------------------------------------------------------
+
+@pytest.fixture
+def force_kernel(monkeypatch):
+    def set_kernel(name):
+        monkeypatch.setenv("PA_DECODE_KERNEL", name)
+    return set_kernel
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+@pytest.mark.parametrize("bs,dtype,H,Hk", [(16, "bf16", 32, 8), (8, "f16", 32, 8), (32, "bf16", 64, 8),
+                                           (128, "bf16", 16, 16), (64, "f16", 48, 4)])
+def test_decode_kernels_against_oracle(pa, force_kernel, kernel, bs, dtype, H, Hk):
+    force_kernel(kernel)
+    rng = np.random.default_rng(bs + H)
+    ctx = np.concatenate([[0, 1, 127, 128, 129, 511, 512, 513, 1500], rng.integers(1, 3000, size=23)]).astype(np.int32)
+    w = workloads.make_decode(f"k_{kernel}", 31, ctx, H, Hk, 128, bs, dtype)
+    out, kc, vc = gpu_decode(w, max_context_len=int(ctx.max()))
+    check_newest_rows(w, kc, vc)
+    ref = oracle_decode(w, range(w.num_seqs))
+    got = to_f64(out)
+    assert np.all(got[0] == 0.0)
+    assert_close(got, ref, dtype, f"{kernel} bs{bs} {dtype} H{H}/{Hk}")
+    _errors_clear(pa)
+
+
+def test_tc_kernel_bad_block_id_reads_zeros(pa, force_kernel):
+    force_kernel("tc")
+    w = workloads.make_decode("badid_tc", 3, np.array([300, 300], np.int32), 8, 2, 128, 16, "bf16")
+    d = dev()
+    kc = torch.zeros((w.num_blocks, 16, 2, 128), dtype=torch.bfloat16, device=d)
+    vc = torch.zeros_like(kc)
+    w.fill_cache_torch(kc, vc, include_newest=True)
+    bad = w.block_tables.copy()
+    bad[1, 3] = -5
+    q = w.q_values(like=kc).to(torch.bfloat16).contiguous()
+    out = torch.empty_like(q)
+    pa.paged_attention_decode(out, q, kc, vc, torch.as_tensor(bad, device=d),
+                              torch.as_tensor(w.context_lens, device=d), w.scale)
+    assert pa.get_device_error() & pa.PA_DEVERR_BLOCK_ID
+    ref = oracle_decode(w, [0])
+    assert_close(to_f64(out)[:1], ref, "bf16", "unaffected sequence")
+    assert torch.isfinite(out.float()).all()
