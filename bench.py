@@ -122,6 +122,22 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """Slowest rank's time (the job is done when the last replica is done)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, step_bytes: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs one replica of the step."""
+    return world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------------------
 # device state of one workload
 # ---------------------------------------------------------------------------
@@ -382,10 +398,7 @@ def run_ours(args):
     clocks = sampler.stop() if sampler is not None else None
     ms = t0.elapsed_time(t1)
     decode_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    if world > 1:
-        tt = torch.tensor([ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, device)
     ms_step = ms / args.steps
 
     # end to end through the public API: pinned host inputs in, result out, every step
@@ -397,7 +410,7 @@ def run_ours(args):
         return
     peak, peak_kind = hbm_peak()
     achieved = st.decode_bytes / (decode_ms * 1e-3) / 1e9
-    value = world * st.step_bytes / (ms_step * 1e-3) / 1e9
+    value = job_gbs(world, st.step_bytes, ms_step)
     w = st.w
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

@@ -81,6 +81,25 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel in the stream is still finishing, so it must execute
+// griddepcontrol.wait before reading anything that kernel (or any earlier work)
+// may write.
+template <typename Kern, typename... Args>
+int launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? 0 : -1;
+}
 constexpr int kMaxDevices = 64;
 
 }  // namespace pa

@@ -15,13 +15,15 @@
 // accumulators in tensor memory. The tensor cores take the G-fold reuse of each
 // K/V element off the FP32 pipes; the kernel stays bound by HBM.
 //
-// CTA = one persistent worker per SM; 192 threads in three roles:
+// CTA = one persistent worker per SM; 224 threads in four roles:
 //   warp 0    TMA producer: per tile, reads the tile's table entries (one lane
 //             per physical block) and loads each block's K and V rows
 //             (box = 64 dims x block_size tokens of one kv head, 128-byte
 //             swizzle) plus the group's queries into a 3-stage ring. Blocks
 //             past the partition end or with a bad id load from an
 //             out-of-range coordinate, which TMA fills with zeros.
+//   warp 6    L2 prefetch: walks the same tiles up to kPrefetchTiles ahead of
+//             the producer's loads and pulls their blocks into L2.
 //   warp 1    MMA issuer (one thread) and tensor-memory owner: S for tile i
 //             into a double-buffered S accumulator, then O for tile i-1 once
 //             its probabilities are in shared memory.
@@ -30,9 +32,9 @@
 //             P^T to shared memory (bf16/f16, 128-byte swizzled K-major), zero
 //             V rows of masked tokens (their contents may be anything), and
 //             o = o * alpha + O_tile in registers.
-// Work items = (sequence, partition, kv head), enumerated from a prefix sum of
-// partitions per sequence built in shared memory at kernel start, assigned to
-// CTAs round-robin. Every wait is bounded (see sm100.cuh); on a timeout the
+// Work items = (sequence, partition, kv head), dealt to CTAs round-robin in
+// order of decreasing size from a bucketed prefix sum that each CTA builds in
+// shared memory at kernel start (see get_item). Every wait is bounded (see sm100.cuh); on a timeout the
 // kernel sets PA_DEVERR_WAIT, drains its copies and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -57,10 +59,11 @@ constexpr int kKVBytes = 2 * kChunkBytes;         // one tile of K (or V), both 
 constexpr int kQBytes = 2 * kN * 128;             // 16 rows x 128 dims
 constexpr int kPBytes = 2 * kN * 128;             // P^T: 16 rows x 128 tokens
 constexpr int kTxBytes = 2 * kKVBytes + kQBytes;  // bytes TMA delivers per stage
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kSoftmaxThreads = 128;
-constexpr int kMaxPrefixSeqs = 2048;
+constexpr int kMaxSeqs = 1024;                    // sequences per launch (the host splits larger batches)
 constexpr uint32_t kTmemCols = 64;                // S[2] x 16 + O[2] x 16 columns
+constexpr int kPrefetchTiles = 2;                 // L2 prefetch distance, in tiles, ahead of the loads
 
 // shared-memory carve-up (from a 1024-aligned base)
 constexpr int kOffK = 0;
@@ -71,9 +74,10 @@ constexpr int kOffRed = kOffP + 2 * kPBytes;                  // float [2][4][16
 constexpr int kOffLRed = kOffRed + 2 * 4 * kN * 4;            // float [4][16]
 constexpr int kOffBar = kOffLRed + 4 * kN * 4;                // uint64 barriers
 constexpr int kNumBars = 4 * kStages + 12;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;              // tmem base, abort flag
-constexpr int kOffPrefix = kOffMisc + 16;                     // int [kMaxPrefixSeqs + 1]
-constexpr int kSmemUsed = kOffPrefix + (kMaxPrefixSeqs + 1) * 4;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;              // tmem base, abort flag, 2 item counts
+constexpr int kOffPrefix = kOffMisc + 32;                     // int [kMaxSeqs + 1]
+constexpr int kOffOrder = kOffPrefix + (kMaxSeqs + 1) * 4;    // int [kMaxSeqs]
+constexpr int kSmemUsed = kOffOrder + kMaxSeqs * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;                  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -89,20 +93,35 @@ struct Item {
     int b, kvh, part, nparts, t0, t1, ntiles;
 };
 
-__device__ __forceinline__ Item get_item(int idx, const int *prefix, const DecodeParams &p) {
+// Items are dealt to CTAs round-robin in order of decreasing size: first every
+// partition with the full tile count (partition_size / 128 tiles: the full ones,
+// and last partitions just as long in tiles), then the other last partitions by
+// tile count -- three or more, two, one -- then empty contexts. prefix[] counts
+// full-tile-count partitions per sequence; order[] lists the remaining sequences
+// in that bucket order (stable within a bucket). n4 = prefix[num_seqs].
+__device__ __forceinline__ Item get_item(int idx, const int *prefix, const int *order, int n4,
+                                         const DecodeParams &p) {
     Item it;
     const int pair = idx / p.num_kv_heads;
     it.kvh = idx - pair * p.num_kv_heads;
-    int lo = 0, hi = p.num_seqs;                  // prefix[lo] <= pair < prefix[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= pair) lo = mid; else hi = mid;
+    int ctx;
+    if (pair < n4) {
+        int lo = 0, hi = p.num_seqs;              // prefix[lo] <= pair < prefix[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= pair) lo = mid; else hi = mid;
+        }
+        it.b = lo;
+        it.part = pair - prefix[lo];
+        ctx = p.context_lens[lo];
+        ctx = ctx < 0 ? 0 : (ctx > p.context_limit ? p.context_limit : ctx);
+    } else {
+        it.b = order[pair - n4];
+        ctx = p.context_lens[it.b];
+        ctx = ctx < 0 ? 0 : (ctx > p.context_limit ? p.context_limit : ctx);
+        it.part = ctx / p.partition_size;        // the sequence's last (ragged) partition
     }
-    it.b = lo;
-    it.part = pair - prefix[lo];
-    it.nparts = prefix[lo + 1] - prefix[lo];
-    int ctx = p.context_lens[lo];
-    ctx = ctx < 0 ? 0 : (ctx > p.context_limit ? p.context_limit : ctx);
+    it.nparts = ctx == 0 ? 1 : (ctx + p.partition_size - 1) / p.partition_size;
     it.t0 = it.part * p.partition_size;
     it.t1 = min(ctx, it.t0 + p.partition_size);
     it.ntiles = it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
@@ -152,6 +171,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     uint64_t *bar_base = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    volatile uint32_t *loads_issued = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc + 16);
     int *prefix = reinterpret_cast<int *>(smem + kOffPrefix);
 
     Bars bars;
@@ -183,6 +203,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         }
         mbar_init(bars.fin, kSoftmaxThreads);
         *abort_flag = 0;
+        *loads_issued = 0;
         mbar_fence_init();
     }
     if (warp == 0 && lane == 0) {
@@ -194,40 +215,87 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    // partitions per sequence -> exclusive prefix sum in shared memory
+    // Programmatic dependent launch: the merge kernel may launch now (it waits for
+    // this grid to finish). Only barrier set-up and the tensor-memory allocation
+    // above overlap the preceding kernel; everything below may read what it wrote.
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // Item order (see get_item): per sequence, the count of full-tile-count
+    // partitions goes to prefix[b + 1] and the list bucket of its last partition to
+    // a byte code (in the P buffer, unused until the first tile); warp 0 then
+    // builds the exclusive prefix sum and the bucketed list, deterministically.
     const int B = p.num_seqs;
+    int *order = reinterpret_cast<int *>(smem + kOffOrder);
+    int *counts = reinterpret_cast<int *>(smem + kOffMisc + 8);   // [0] = n4, [1] = list length
+    unsigned char *code = sP;
     for (int b = tid; b < B; b += kThreads) {
         int ctx = p.context_lens[b];
         if (ctx < 0 || ctx > p.context_limit) {
             if (blockIdx.x == 0) raise_error(p.err, PA_DEVERR_CONTEXT);
             ctx = ctx < 0 ? 0 : p.context_limit;
         }
-        prefix[b + 1] = ctx == 0 ? 1 : (ctx + p.partition_size - 1) / p.partition_size;
+        const int nfull = ctx / p.partition_size;
+        const int rt = (ctx - nfull * p.partition_size + kTile - 1) / kTile;   // tiles of the ragged rest
+        const bool rest_is_full = rt * kTile == p.partition_size;           // as many tiles as a full one
+        prefix[b + 1] = nfull + (rest_is_full ? 1 : 0);
+        // list bucket: 0 = empty context, 1..3 = tiles of the rest (3 = three or more),
+        // 4 = no list entry (no ragged rest, or one with the full tile count)
+        code[b] = (unsigned char)(ctx == 0 ? 0 : ((rt == 0 || rest_is_full) ? 4 : min(rt, 3)));
     }
     __syncthreads();
     if (warp == 0) {
         const int per = (B + 31) / 32;
-        const int lo = 1 + lane * per, hi = min(B + 1, lo + per);
-        int sum = 0;
-        for (int i = lo; i < hi; ++i) sum += prefix[i];
-        int incl = sum;
+        const int lo = lane * per, hi = min(B, lo + per);
+        int s4 = 0, c0 = 0, c1 = 0, c2 = 0, c3 = 0;        // this lane's counts per bucket
+        for (int i = lo; i < hi; ++i) {
+            s4 += prefix[i + 1];
+            const int k = code[i];
+            c0 += k == 0;
+            c1 += k == 1;
+            c2 += k == 2;
+            c3 += k == 3;
+        }
+        int i4 = s4, i0 = c0, i1 = c1, i2 = c2, i3 = c3;     // inclusive scans over lanes
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
+            const int n4v = __shfl_up_sync(0xffffffffu, i4, o), n0 = __shfl_up_sync(0xffffffffu, i0, o);
+            const int n1 = __shfl_up_sync(0xffffffffu, i1, o), n2 = __shfl_up_sync(0xffffffffu, i2, o);
+            const int n3 = __shfl_up_sync(0xffffffffu, i3, o);
+            if (lane >= o) {
+                i4 += n4v;
+                i0 += n0;
+                i1 += n1;
+                i2 += n2;
+                i3 += n3;
+            }
         }
-        int run = incl - sum;
+        const int t0 = __shfl_sync(0xffffffffu, i0, 31), t1 = __shfl_sync(0xffffffffu, i1, 31);
+        const int t2 = __shfl_sync(0xffffffffu, i2, 31), t3 = __shfl_sync(0xffffffffu, i3, 31);
+        // list order: bucket 3, 2, 1, then 0
+        int p3 = i3 - c3, p2 = t3 + i2 - c2, p1 = t3 + t2 + i1 - c1, p0 = t3 + t2 + t1 + i0 - c0;
+        int run = i4 - s4;
         for (int i = lo; i < hi; ++i) {
-            run += prefix[i];
-            prefix[i] = run;
+            run += prefix[i + 1];
+            prefix[i + 1] = run;
+            const int k = code[i];
+            if (k == 3) order[p3++] = i;
+            else if (k == 2) order[p2++] = i;
+            else if (k == 1) order[p1++] = i;
+            else if (k == 0) order[p0++] = i;
         }
         if (lane == 0) prefix[0] = 0;
+        if (lane == 31) {
+            counts[0] = i4;
+            counts[1] = t0 + t1 + t2 + t3;
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int total_items = prefix[B] * p.num_kv_heads;
+    const int n4 = counts[0];
+    const int total_items = (counts[0] + counts[1]) * p.num_kv_heads;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -235,7 +303,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         uint32_t it = 0;
         bool ok = true;
         for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-            const Item I = get_item(idx, prefix, p);
+            const Item I = get_item(idx, prefix, order, n4, p);
             const int32_t *table = p.block_tables + (int64_t)I.b * p.max_blocks_per_seq;
             const int qrow = I.b * p.num_heads + I.kvh * G;
             for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
@@ -272,6 +340,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                     unsigned char *dq = sQ + stage * kQBytes;
                     tma_load_2d(dq, &tm_q, &bars.full[stage], 0, qrow);
                     tma_load_2d(dq + kN * 128, &tm_q, &bars.full[stage], 64, qrow);
+                    *loads_issued = it + 1;             // tiles whose loads are issued
                 }
             }
         }
@@ -315,7 +384,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                 return true;
             };
             for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-                const Item I = get_item(idx, prefix, p);
+                const Item I = get_item(idx, prefix, order, n4, p);
                 for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
                     const int stage = it % kStages, buf = it & 1;
                     if (*abort_flag || !mbar_wait(&bars.full[stage], (it / kStages) & 1) ||
@@ -351,6 +420,43 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             }
         }
         __syncwarp();
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ L2 prefetch
+        // Walks the same tiles as the producer, at most kPrefetchTiles ahead of its
+        // loads, pulling each tile's blocks into L2 so that the ring's loads find
+        // them there. Prefetches are hints: if this warp falls behind or gives up,
+        // only speed changes.
+        const int nbt = kTile / p.block_size;
+        uint32_t n = 0;
+        bool go = true;
+        for (int idx = blockIdx.x; idx < total_items && go; idx += gridDim.x) {
+            const Item I = get_item(idx, prefix, order, n4, p);
+            const int32_t *table = p.block_tables + (int64_t)I.b * p.max_blocks_per_seq;
+            for (int tile = 0; tile < I.ntiles; ++tile, ++n) {
+                int e = -1;
+                if (lane < nbt) {
+                    const int tok = I.t0 + tile * kTile + lane * p.block_size;
+                    if (tok < I.t1) e = table[tok >> p.log2_block_size];
+                }
+                if (n >= *loads_issued + kPrefetchTiles) {
+                    const unsigned long long t0 = globaltimer_ns();
+                    while (n >= *loads_issued + kPrefetchTiles) {
+                        if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+                            go = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!go) break;
+                }
+                if (e >= 0 && e < p.num_blocks) {
+                    tma_prefetch_4d(&tm_k, 0, I.kvh, 0, e);
+                    tma_prefetch_4d(&tm_k, 64, I.kvh, 0, e);
+                    tma_prefetch_4d(&tm_v, 0, I.kvh, 0, e);
+                    tma_prefetch_4d(&tm_v, 64, I.kvh, 0, e);
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ softmax / output
         const int q4 = warp & 3;                       // tensor-memory lane quadrant
@@ -361,7 +467,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         bool ok = true;
         float m_run[GT], l_part[GT], o_acc[GT], alpha_prev[GT];
         for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-            const Item I = get_item(idx, prefix, p);
+            const Item I = get_item(idx, prefix, order, n4, p);
             const int64_t head0 = (int64_t)I.b * p.num_heads + (int64_t)I.kvh * G;
             if (I.ntiles == 0) {
 #pragma unroll
@@ -575,8 +681,7 @@ int launch_tc_t(const DecodeParams &p, CUtensorMapDataType dt, cudaStream_t stre
         return -1;
     const int64_t max_items = (int64_t)p.num_seqs * p.num_kv_heads * p.max_partitions;
     const int grid = (int)(max_items < num_sms[dev] ? max_items : num_sms[dev]);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, mq, p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, stream, mk, mv, mq, p);
 }
 
 template <typename T>
@@ -591,14 +696,31 @@ int launch_tc_g(const DecodeParams &p, CUtensorMapDataType dt, cudaStream_t stre
 bool decode_tc_supported(const DecodeParams &p, int dtype) {
     return (dtype == PA_DTYPE_BF16 || dtype == PA_DTYPE_F16) && p.head_dim == kD && p.group >= 1 &&
            p.group <= kN && p.block_size >= 8 && p.block_size <= kTile && p.partition_size % kTile == 0 &&
-           p.num_seqs <= kMaxPrefixSeqs && p.num_blocks < INT32_MAX &&
-           (int64_t)p.num_seqs * p.num_heads < INT32_MAX;
+           p.num_blocks < INT32_MAX && (int64_t)p.num_seqs * p.num_heads < INT32_MAX;
 }
 
+// Batches above kMaxSeqs sequences run as independent launches of up to kMaxSeqs
+// sequences (the sequences share nothing but the cache).
 int launch_decode_tc(const DecodeParams &p, int dtype, cudaStream_t stream) {
     if (!decode_tc_supported(p, dtype)) return -2;
-    if (dtype == PA_DTYPE_BF16) return launch_tc_g<__nv_bfloat16>(p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, stream);
-    return launch_tc_g<__half>(p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, stream);
+    for (int b0 = 0; b0 < p.num_seqs; b0 += kMaxSeqs) {
+        DecodeParams c = p;
+        const int64_t rows = (int64_t)b0 * p.num_heads;
+        c.num_seqs = min(kMaxSeqs, p.num_seqs - b0);
+        c.q = static_cast<const char *>(p.q) + rows * kD * 2;
+        c.out = static_cast<char *>(p.out) + rows * kD * 2;
+        c.block_tables = p.block_tables + (int64_t)b0 * p.max_blocks_per_seq;
+        c.context_lens = p.context_lens + b0;
+        if (p.ws_ml) {
+            c.ws_ml = p.ws_ml + rows * p.max_partitions * 2;
+            c.ws_o = p.ws_o + rows * p.max_partitions * kD;
+        }
+        const int rc = dtype == PA_DTYPE_BF16
+                           ? launch_tc_g<__nv_bfloat16>(c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, stream)
+                           : launch_tc_g<__half>(c, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, stream);
+        if (rc != 0) return rc;
+    }
+    return 0;
 }
 
 }  // namespace pa

@@ -27,6 +27,9 @@ __global__ __launch_bounds__(kWriteWarps * 32) void kv_write_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int32_t *__restrict__ slots,
     int64_t num_tokens, uint4 *__restrict__ kc, uint4 *__restrict__ vc, int64_t num_slots,
     int row_vecs, unsigned int *err) {
+    // a decode launched after this kernel may start its set-up now; it waits for
+    // this grid to finish before reading the cache
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
     if (t >= num_tokens) return;

@@ -409,3 +409,15 @@ def test_tc_kernel_bad_block_id_reads_zeros(pa, force_kernel):
     ref = oracle_decode(w, [0])
     assert_close(to_f64(out)[:1], ref, "bf16", "unaffected sequence")
     assert torch.isfinite(out.float()).all()
+
+
+def test_large_batch_runs_in_chunks(pa):
+    # more than 1024 sequences: the tensor-core path runs independent launches
+    rng = np.random.default_rng(41)
+    ctx = rng.integers(0, 1200, size=2500).astype(np.int32)
+    w = workloads.make_decode("big_batch", 41, ctx, 16, 4, 128, 16, "bf16")
+    out, kc, vc = gpu_decode(w, max_context_len=int(ctx.max()), partition_size=256)
+    seqs = np.concatenate([np.arange(0, 2500, 37), [1023, 1024, 1025, 2047, 2048, 2499]])
+    ref = oracle_decode(w, seqs)
+    assert_close(to_f64(out)[seqs], ref, "bf16", "2500 sequences")
+    _errors_clear(pa)
