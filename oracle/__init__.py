@@ -13,6 +13,9 @@ What it computes and where that is defined (web pages, by title and section):
   - decode attention: "CS349E lecture 7: 01_paged_attention.py", demo 2,
     paper eq. 4 (block-wise scores, one softmax over the whole context,
     block-wise V accumulation, equal to contiguous attention);
+  - chunked-prefill attention: the same per query position, each seeing the
+    positions up to its own (demo 1/demo 2 paged steps; "04 - Paged Attention
+    实现进度", B.2 and D.2, cu_seqlens_q / query_start_loc);
   - block manager: see ``allocator_model.py``.
 
 Every function is pinned by tests in ``tests/test_oracle_pins.py`` against
@@ -72,6 +75,9 @@ def _load():
                                                  i32p, c_int, c_int, c_int, c_int, c_int, i64,
                                                  ctypes.c_double, c_int, c_int]
         lib.oracle_attention_weights.restype = c_int
+        lib.oracle_paged_prefill.argtypes = [vp, vp, vp, vp, c_int, i32p, c_int, i32p, i32p, c_int, c_int,
+                                             c_int, c_int, c_int, i64, ctypes.c_double, c_int]
+        lib.oracle_paged_prefill.restype = c_int
         _lib = lib
     return _lib
 
@@ -168,6 +174,29 @@ def attention_weights(q, key_cache, value_cache, block_tables, context_lens, sca
     if rc != 0:
         raise ValueError(f"oracle_attention_weights: {rc}")
     return w[: int(cl[b])], out
+
+
+def paged_prefill(q, key_cache, value_cache, block_tables, context_lens, query_start_loc, scale: float,
+                  dtype: str, num_threads: int = 1) -> np.ndarray:
+    """float64 out [total_q, H, D] of causal chunked-prefill attention over a paged cache."""
+    lib = _load()
+    q = _check_storage(q, dtype)
+    kc = _check_storage(key_cache, dtype)
+    vc = _check_storage(value_cache, dtype)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    T, H, D = q.shape
+    nb, bs, hk, d2 = kc.shape
+    B = cl.shape[0]
+    if d2 != D or vc.shape != kc.shape or bt.shape[0] != B or qs.shape[0] != B + 1 or qs[-1] != T:
+        raise ValueError("shape mismatch")
+    out = np.zeros((T, H, D), dtype=np.float64)
+    rc = lib.oracle_paged_prefill(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _CODES[dtype], _ptr(bt), bt.shape[1],
+                                  _ptr(cl), _ptr(qs), B, H, hk, D, bs, nb, float(scale), int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_prefill: {rc}")
+    return out
 
 
 def num_host_threads() -> int:

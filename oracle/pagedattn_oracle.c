@@ -17,7 +17,9 @@
  *       the result equals attention over the concatenated (contiguous) K/V.
  *  [P3] "04 - Paged Attention 实现进度", section B.2: slot_mapping maps each new
  *       token to a physical slot (block id + offset), block_tables has shape
- *       [batch, max_blocks_per_seq], context_lens is each sequence's length.
+ *       [batch, max_blocks_per_seq], context_lens is each sequence's length,
+ *       cu_seqlens_q (query_start_loc in vLLM's terms, section D.2) packs the
+ *       variable-length query chunks of a prefill step.
  *
  * Readings where the pages are silent (each one is listed in the design notes):
  *  - slot = physical_block * block_size + offset; slot -1 means "skip".
@@ -340,4 +342,148 @@ int oracle_attention_weights(double *weights, double *out, const void *q, int q_
     J.num_blocks = num_blocks; J.scale = scale;
     J.weights = weights; J.weights_b = b; J.weights_h = h;
     return run_attention(&J, 1);
+}
+
+/* ------------------------------------------------------------------------
+ * Chunked-prefill attention over a paged cache  [P2 demo 1 and demo 2: a
+ * paged step first writes the chunk's K/V, then every position of the chunk
+ * attends; P3 B.2: cu_seqlens_q packs the chunks]
+ *
+ * Sequence b owns query rows query_start_loc[b] .. query_start_loc[b+1]-1
+ * (q_len_b rows). Its context holds context_lens[b] tokens, the chunk being the
+ * last q_len_b of them, so query row i sits at position
+ * pos = context_lens[b] - q_len_b + i and sees positions 0..pos (causal). For
+ * each query head h (kv head h / G): gather K, V of positions 0..pos through the
+ * block table, s[t] = scale * q . K[t], p = softmax(s), out = sum_t p[t] V[t].
+ * q, out: [total_q, num_heads, head_dim].
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    double *out;
+    const void *q;
+    int dtype;
+    const void *key_cache, *value_cache;
+    const int32_t *block_tables;
+    int max_blocks_per_seq;
+    const int32_t *context_lens, *query_start_loc;
+    int num_seqs, num_heads, num_kv_heads, head_dim, block_size;
+    int64_t num_blocks;
+    double scale;
+    int64_t next_item;
+    int status;
+} prefill_job;
+
+static void *prefill_worker(void *arg)
+{
+    prefill_job *J = (prefill_job *)arg;
+    const int D = J->head_dim, Hk = J->num_kv_heads, bs = J->block_size, H = J->num_heads;
+    const int G = H / Hk;
+    const int64_t row = (int64_t)Hk * D;
+    int max_ctx = 1;
+    for (int b = 0; b < J->num_seqs; ++b)
+        if (J->context_lens[b] > max_ctx)
+            max_ctx = J->context_lens[b];
+    double *Kc = malloc(sizeof(double) * (size_t)max_ctx * (size_t)D);
+    double *Vc = malloc(sizeof(double) * (size_t)max_ctx * (size_t)D);
+    double *s = malloc(sizeof(double) * (size_t)max_ctx);
+    if (!Kc || !Vc || !s) {
+        __atomic_store_n(&J->status, OR_ERR_NOMEM, __ATOMIC_RELAXED);
+        free(Kc); free(Vc); free(s);
+        return NULL;
+    }
+    const int64_t items = (int64_t)J->num_seqs * Hk;
+    for (;;) {
+        int64_t it = __atomic_fetch_add(&J->next_item, 1, __ATOMIC_RELAXED);
+        if (it >= items)
+            break;
+        const int b = (int)(it / Hk), kvh = (int)(it % Hk);
+        const int ctx = J->context_lens[b];
+        const int q0 = J->query_start_loc[b], q_len = J->query_start_loc[b + 1] - q0;
+        int bad = 0;
+        /* gather the whole context once; each query uses a prefix of it */
+        for (int t = 0; t < ctx && !bad; ++t) {
+            int32_t phys = J->block_tables[(int64_t)b * J->max_blocks_per_seq + t / bs];
+            if (phys < 0 || phys >= J->num_blocks) {
+                bad = 1;
+                break;
+            }
+            int64_t base = ((int64_t)phys * bs + t % bs) * row + (int64_t)kvh * D;
+            for (int d = 0; d < D; ++d) {
+                Kc[(int64_t)t * D + d] = load_elem(J->key_cache, base + d, J->dtype);
+                Vc[(int64_t)t * D + d] = load_elem(J->value_cache, base + d, J->dtype);
+            }
+        }
+        if (bad) {
+            __atomic_store_n(&J->status, OR_ERR_BLOCK_ID, __ATOMIC_RELAXED);
+            continue;
+        }
+        for (int i = 0; i < q_len; ++i) {
+            const int n = ctx - q_len + i + 1;            /* positions 0..pos */
+            for (int g = 0; g < G; ++g) {
+                const int h = kvh * G + g;
+                const int64_t qbase = ((int64_t)(q0 + i) * H + h) * D;
+                double *o = J->out + qbase;
+                for (int t = 0; t < n; ++t) {
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        acc += load_elem(J->q, qbase + d, J->dtype) * Kc[(int64_t)t * D + d];
+                    s[t] = J->scale * acc;
+                }
+                double m = s[0];
+                for (int t = 1; t < n; ++t)
+                    if (s[t] > m)
+                        m = s[t];
+                double l = 0.0;
+                for (int t = 0; t < n; ++t) {
+                    s[t] = exp(s[t] - m);
+                    l += s[t];
+                }
+                for (int t = 0; t < n; ++t)
+                    s[t] = s[t] / l;
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int t = 0; t < n; ++t)
+                        acc += s[t] * Vc[(int64_t)t * D + d];
+                    o[d] = acc;
+                }
+            }
+        }
+    }
+    free(Kc); free(Vc); free(s);
+    return NULL;
+}
+
+int oracle_paged_prefill(double *out, const void *q, const void *key_cache, const void *value_cache,
+                         int dtype, const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, const int32_t *query_start_loc, int num_seqs,
+                         int num_heads, int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks, double scale, int num_threads)
+{
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_heads % num_kv_heads != 0 || elem_bytes(dtype) == 0)
+        return OR_ERR_ARG;
+    for (int b = 0; b < num_seqs; ++b) {
+        const int q_len = query_start_loc[b + 1] - query_start_loc[b];
+        if (q_len < 0 || context_lens[b] < q_len)
+            return OR_ERR_ARG;
+        if ((int64_t)context_lens[b] > (int64_t)max_blocks_per_seq * block_size)
+            return OR_ERR_CONTEXT;
+    }
+    prefill_job J;
+    memset(&J, 0, sizeof J);
+    J.out = out; J.q = q; J.dtype = dtype; J.key_cache = key_cache; J.value_cache = value_cache;
+    J.block_tables = block_tables; J.max_blocks_per_seq = max_blocks_per_seq;
+    J.context_lens = context_lens; J.query_start_loc = query_start_loc; J.num_seqs = num_seqs;
+    J.num_heads = num_heads; J.num_kv_heads = num_kv_heads; J.head_dim = head_dim;
+    J.block_size = block_size; J.num_blocks = num_blocks; J.scale = scale;
+    if (num_threads < 1) num_threads = 1;
+    if (num_threads > 256) num_threads = 256;
+    pthread_t tid[256];
+    int started = 0;
+    for (int i = 1; i < num_threads; ++i)
+        if (pthread_create(&tid[started], NULL, prefill_worker, &J) == 0)
+            started++;
+    prefill_worker(&J);
+    for (int i = 0; i < started; ++i)
+        pthread_join(tid[i], NULL);
+    return J.status;
 }

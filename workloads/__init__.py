@@ -514,3 +514,91 @@ WORKLOADS = {
     "shared_prefix": shared_prefix,
     "mixed_serving": mixed_serving,
 }
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill
+# ---------------------------------------------------------------------------
+
+@dataclass
+class PrefillWorkload:
+    """A chunked-prefill batch on top of a decode-style layout.
+
+    ``base`` holds the contexts *including* each sequence's chunk, so its
+    block tables, pool and token contents apply unchanged; sequence b's chunk is
+    its last q_lens[b] positions. Query rows are packed in sequence order;
+    query_start_loc[b] is the first row of sequence b."""
+    base: DecodeWorkload
+    q_lens: np.ndarray                 # int32 [B]
+
+    @property
+    def query_start_loc(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.q_lens)]).astype(np.int32)
+
+    @property
+    def total_q(self) -> int:
+        return int(self.q_lens.sum())
+
+    def chunk_index(self):
+        """(seq_idx, pos) int64 arrays of every query row, in packed order."""
+        ctx = self.base.context_lens.astype(np.int64)
+        ql = self.q_lens.astype(np.int64)
+        seq_idx = np.repeat(np.arange(ctx.shape[0], dtype=np.int64), ql)
+        starts = np.repeat(np.cumsum(ql) - ql, ql)
+        i = np.arange(int(ql.sum()), dtype=np.int64) - starts
+        return seq_idx, ctx[seq_idx] - ql[seq_idx] + i
+
+    def q_values(self, like=None):
+        """float32 [total_q, H, D] queries (q_mult applied)."""
+        w = self.base
+        seq_idx, pos = self.chunk_index()
+        keys = w.own_key[seq_idx]
+        if like is not None and _is_torch(like):
+            import torch
+            keys = torch.as_tensor(keys, device=like.device)
+            pos = torch.as_tensor(pos + 1, device=like.device)
+        else:
+            pos = pos + 1
+        rows = content_rows(w.seed, TID_Q, keys, pos, w.num_heads * w.head_dim)
+        return (rows * w.q_mult).reshape(-1, w.num_heads, w.head_dim)
+
+    def chunk_kv(self, like=None):
+        """K, V rows [total_q, Hk, D] of the chunk positions (written before attending)."""
+        w = self.base
+        seq_idx, pos = self.chunk_index()
+        if like is not None and _is_torch(like):
+            import torch
+            seq_idx = torch.as_tensor(seq_idx, device=like.device)
+            pos = torch.as_tensor(pos, device=like.device)
+        shp = (-1, w.num_kv_heads, w.head_dim)
+        return w.kv_rows(TID_K, seq_idx, pos).reshape(shp), w.kv_rows(TID_V, seq_idx, pos).reshape(shp)
+
+    def chunk_slots(self) -> np.ndarray:
+        seq_idx, pos = self.chunk_index()
+        return self.base._slots(seq_idx, pos).astype(np.int32)
+
+    def flops(self) -> int:
+        """Scores plus weighted sum: 4 * D flops per (query row, head, visible key)."""
+        w = self.base
+        ctx = w.context_lens.astype(np.int64)
+        ql = self.q_lens.astype(np.int64)
+        visible = (ctx - ql) * ql + ql * (ql + 1) // 2
+        return int(4 * w.head_dim * w.num_heads * visible.sum())
+
+
+def make_prefill(name: str, seed: int, prior: np.ndarray, q_lens: np.ndarray, num_heads: int,
+                 num_kv_heads: int, head_dim: int, block_size: int, dtype: str) -> PrefillWorkload:
+    """Sequences with `prior` cached tokens each receiving a chunk of q_lens tokens."""
+    prior = np.asarray(prior, dtype=np.int32)
+    q_lens = np.asarray(q_lens, dtype=np.int32)
+    base = make_decode(name, seed, prior + q_lens, num_heads, num_kv_heads, head_dim, block_size, dtype)
+    return PrefillWorkload(base=base, q_lens=q_lens)
+
+
+def chunked_prefill(seed: int = 1006, num_seqs: int = 16, chunk: int = 512,
+                    dtype: str = "bf16") -> PrefillWorkload:
+    """16 sequences, each with U[0, 3584] cached tokens and a 512-token chunk;
+    32 q heads / 8 kv heads, head_dim 128, bf16, block_size 16."""
+    rng = np.random.default_rng(seed)
+    prior = rng.integers(0, 3585, size=num_seqs)
+    return make_prefill("chunked_prefill", seed, prior, np.full(num_seqs, chunk), 32, 8, 128, 16, dtype)
