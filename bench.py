@@ -6,7 +6,7 @@ copy-on-write block copies when the workload has them (copy_blocks), and decode
 attention over the paged cache (split-K partition kernel + merge kernel).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload llama8b_decode|long_context|mixed_serving|shared_prefix]
+                  [--workload llama8b_decode|long_context|mixed_serving|shared_prefix|chunked_prefill]
 
 Prints one JSON line (rank 0). ``value`` is algorithmic bytes per step (K and V
 of every context once, q, out, the table entries and lengths used, plus the
@@ -256,6 +256,101 @@ class Step:
                       f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"}
 
 
+class PrefillStep:
+    """Chunked-prefill step: scatter the chunk's K/V, then every chunk row attends."""
+
+    def __init__(self, device):
+        import torch
+
+        import paged_kv_cache_261_gb300 as pa
+        self.pa = pa
+        self.name = "chunked_prefill"
+        self.pw = pw = workloads.chunked_prefill()
+        w = pw.base
+        self.w = w
+        dt = workloads.torch_dtype(w.dtype)
+        shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+        self.kc = torch.zeros(shape, dtype=dt, device=device)
+        self.vc = torch.zeros(shape, dtype=dt, device=device)
+        workloads.fill_prior_torch(pw, self.kc, self.vc)
+        k, v = pw.chunk_kv(like=self.kc)
+        self.k_new, self.v_new = k.to(dt).contiguous(), v.to(dt).contiguous()
+        self.slots = torch.as_tensor(pw.chunk_slots(), device=device)
+        self.q = pw.q_values(like=self.kc).to(dt).contiguous()
+        self.out = torch.empty_like(self.q)
+        self.bt = torch.as_tensor(w.block_tables, device=device)
+        self.cl = torch.as_tensor(w.context_lens, device=device)
+        self.qs = torch.as_tensor(pw.query_start_loc, device=device)
+        self.max_q = int(pw.q_lens.max())
+        self.flops = pw.flops()
+        self.launches_per_step = 2
+        torch.cuda.synchronize()
+
+    def run(self, ev=None):
+        pa = self.pa
+        pa.paged_kv_write(self.k_new, self.v_new, self.slots, self.kc, self.vc)
+        if ev is not None:
+            ev[0].record()
+        pa.paged_attention_prefill(self.out, self.q, self.kc, self.vc, self.bt, self.cl, self.qs, self.w.scale,
+                                   self.max_q)
+        if ev is not None:
+            ev[1].record()
+
+    def config(self):
+        w, pw = self.w, self.pw
+        return {"workload": self.name, "num_seqs": w.num_seqs, "num_heads": w.num_heads,
+                "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                "query_tokens": pw.total_q, "chunk": self.max_q,
+                "prior_min": int((w.context_lens - pw.q_lens).min()),
+                "prior_max": int((w.context_lens - pw.q_lens).max()),
+                "l2": "K/V of the batch fit in L2 across a step; no flush (tensor-bound kernel)"}
+
+
+def run_prefill(args, device, rank, world):
+    """Timed loop of the chunked-prefill step (TFLOP/s of causal attention)."""
+    import torch
+    st = PrefillStep(device)
+    for _ in range(max(args.warmup, 3)):
+        st.run()
+    torch.cuda.synchronize()
+    if st.pa.get_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(None) if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(args.steps):
+        st.run(evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler is not None else None
+    ms = max_over_ranks(t0.elapsed_time(t1), device) / args.steps
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except Exception:
+        pass
+    peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    achieved = st.flops / (kern_ms * 1e-3) / 1e12
+    line = {"metric": "paged chunked-prefill attention TFLOP/s on 1×GB300 (causal, packed chunks)",
+            "value": world * st.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": st.w.dtype, "data": "synthetic",
+            "config": st.config(), "tokens_per_s": world * st.pw.total_q / (ms * 1e-3),
+            "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
+                         "peak_kind": "measured bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks
+                         else "fallback", "unit": "TFLOP/s", "frac": achieved / peak,
+                         "algorithmic_flops_per_launch": st.flops, "kernel_ms": kern_ms, "traffic": None},
+            "gpu_launches": st.launches_per_step * args.steps, "clocks": clocks}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
@@ -367,6 +462,11 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
 
+    if args.workload == "chunked_prefill":
+        run_prefill(args, device, rank, world)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     st = Step(args.workload, device)
     for _ in range(max(args.warmup, 3)):
         st.run()
@@ -482,7 +582,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode",
-                    choices=["llama8b_decode", "long_context", "mixed_serving", "shared_prefix"])
+                    choices=["llama8b_decode", "long_context", "mixed_serving", "shared_prefix",
+                             "chunked_prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -141,6 +141,40 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
                               size_t workspace_bytes, int dtype, void *stream);
 
 /*
+ * Chunked-prefill attention over the paged cache.
+ * [P2 demo 1 and demo 2: a paged step writes the chunk's K/V into its blocks,
+ *  then every position of the chunk attends to the positions up to its own;
+ *  P3 B.2 and D.2: cu_seqlens_q (query_start_loc) packs the chunks of a batch]
+ *
+ * Sequence b owns query rows query_start_loc[b] .. query_start_loc[b+1]-1 of
+ * q and out ([num_query_tokens, num_heads, head_dim]); q_len_b is their count.
+ * Its context holds context_lens[b] tokens whose last q_len_b are the chunk
+ * (already written, e.g. with pa_paged_kv_write). Row i sits at position
+ * pos = context_lens[b] - q_len_b + i and
+ *
+ *   out[row, h, :] = sum_{t <= pos} softmax_t(scale * q[row, h, :] . K[b,t,h/G,:]) V[b,t,h/G,:].
+ *
+ * Accumulation is fp32 (probabilities rounded to the cache type for the
+ * P.V product). max_query_len is a host-side bound on every q_len_b; it sizes
+ * the grid. A sequence with q_len_b < 0, q_len_b > max_query_len,
+ * q_len_b > context_lens[b], context_lens[b] > max_blocks_per_seq*block_size,
+ * or rows outside [0, num_query_tokens) sets PA_DEVERR_CONTEXT and its rows are
+ * left unwritten; a live table entry outside [0, num_blocks) sets
+ * PA_DEVERR_BLOCK_ID and reads as zeros.
+ *
+ * Supported: dtype f16/bf16, head_dim 128, num_heads/num_kv_heads <= 16,
+ * block_size a power of two in [8, 128]; else PA_ERR_UNSUPPORTED.
+ * Allocates nothing.
+ */
+int pa_paged_attention_prefill(void *out, const void *q, const void *key_cache,
+                               const void *value_cache, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *context_lens,
+                               const int32_t *query_start_loc, int num_seqs,
+                               int64_t num_query_tokens, int max_query_len, int num_heads,
+                               int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, float scale, int dtype, void *stream);
+
+/*
  * Decode attention that allocates no device memory. The paper has no
  * counterpart to this entry point; it exists for callers, not for the method.
  *

@@ -10,6 +10,8 @@ Entry points (same names as the C ABI, without the ``pa_`` prefix):
   paged_kv_write(k, v, slot_mapping, key_cache, value_cache)
   paged_attention_decode(out, q, key_cache, value_cache, block_tables,
                          context_lens, scale, block_size, num_kv_heads)
+  paged_attention_prefill(out, q, key_cache, value_cache, block_tables,
+                          context_lens, query_start_loc, scale, max_query_len)
   copy_blocks(key_cache, value_cache, src_dst_pairs)
   get_device_error()
   BlockAllocator: the host block manager (free list, reference counts, fork,
@@ -69,6 +71,8 @@ _decl("pa_paged_attention_decode", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i
                                     _i64, _f, _i32, _i32, _vp, _sz, _i32, _vp])
 _decl("pa_copy_blocks", [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp])
 _decl("pa_get_device_error", [_vp, ctypes.POINTER(ctypes.c_uint32)])
+_decl("pa_paged_attention_prefill", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
+                                     _i32, _i64, _f, _i32, _vp])
 
 
 class PagedAttnError(RuntimeError):
@@ -217,6 +221,37 @@ def paged_attention_decode(out, q, key_cache, value_cache, block_tables, context
                                         int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
                                         _dtype_code(key_cache), sp)
     _check(rc, "pa_paged_attention_decode")
+
+
+def paged_attention_prefill(out, q, key_cache, value_cache, block_tables, context_lens, query_start_loc,
+                            scale: float, max_query_len: int, stream=None) -> None:
+    """Causal chunked-prefill attention: q, out [T, H, D] packed by query_start_loc [B + 1];
+    row i of sequence b sits at position context_lens[b] - q_len_b + i and sees
+    positions up to its own. max_query_len: host bound on every chunk length."""
+    torch = _torch()
+    dev = key_cache.device
+    _cuda(key_cache, "key_cache")
+    _cuda(value_cache, "value_cache", key_cache.dtype, dev)
+    _cuda(q, "q", key_cache.dtype, dev)
+    _cuda(out, "out", key_cache.dtype, dev)
+    _cuda(block_tables, "block_tables", torch.int32, dev)
+    _cuda(context_lens, "context_lens", torch.int32, dev)
+    _cuda(query_start_loc, "query_start_loc", torch.int32, dev)
+    nb, bs, hk, d = key_cache.shape
+    if value_cache.shape != key_cache.shape:
+        raise ValueError("value_cache shape differs from key_cache")
+    T, H, D = q.shape
+    B = context_lens.shape[0]
+    if D != d or tuple(out.shape) != (T, H, D):
+        raise ValueError("q/out must be [T, H, head_dim]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(query_start_loc.shape) != (B + 1,):
+        raise ValueError("block_tables must be [B, MB] and query_start_loc [B + 1]")
+    rc = _lib.pa_paged_attention_prefill(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
+                                         value_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+                                         context_lens.data_ptr(), query_start_loc.data_ptr(), B, T,
+                                         int(max_query_len), H, hk, D, bs, nb, float(scale),
+                                         _dtype_code(key_cache), _stream_ptr(stream, dev))
+    _check(rc, "pa_paged_attention_prefill")
 
 
 def copy_blocks(key_cache, value_cache, src_dst_pairs, stream=None) -> None:

@@ -209,6 +209,59 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
     return rc == 0 ? PA_OK : PA_ERR_CUDA;
 }
 
+int pa_paged_attention_prefill(void *out, const void *q, const void *key_cache, const void *value_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                               const int32_t *query_start_loc, int num_seqs, int64_t num_query_tokens,
+                               int max_query_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, float scale, int dtype, void *stream) {
+    if (elem_size(dtype) == 0 || num_seqs < 0 || num_query_tokens < 0 || max_query_len < 0 || num_heads <= 0 ||
+        num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (dtype == PA_DTYPE_F32 || head_dim != 128 || num_heads / num_kv_heads > 16 || !pow2(block_size) ||
+        block_size < 8 || block_size > 128)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_query_tokens == 0 || max_query_len == 0) return PA_OK;
+    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens || !query_start_loc)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+    const int64_t table_cap = (int64_t)max_blocks_per_seq * block_size;
+    if (table_cap > INT32_MAX || num_query_tokens > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    pa::PrefillParams p{};
+    p.out = out;
+    p.q = q;
+    p.key_cache = key_cache;
+    p.value_cache = value_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.query_start_loc = query_start_loc;
+    p.num_blocks = num_blocks;
+    p.num_query_tokens = num_query_tokens;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_heads / num_kv_heads;
+    int gp = 1;
+    while (gp < p.group) gp <<= 1;
+    p.group_pad = gp;
+    p.rows_q = 128 / gp;
+    p.qtiles = (max_query_len + p.rows_q - 1) / p.rows_q;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.log2_block_size = ilog2(block_size);
+    p.max_query_len = max_query_len;
+    p.context_limit = (int)table_cap;
+    p.scale_log2 = scale * pa::kLog2e;
+    if ((int64_t)num_seqs * num_kv_heads * p.qtiles > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    if (int rc = error_word(&p.err)) return rc;
+    const int rc = pa::launch_prefill_tc(p, dtype, static_cast<cudaStream_t>(stream));
+    if (rc == -2) return PA_ERR_UNSUPPORTED;
+    return rc == 0 ? PA_OK : PA_ERR_CUDA;
+}
+
 int pa_copy_blocks(void *key_cache, void *value_cache, const int32_t *src_dst_pairs, int64_t num_pairs,
                    int64_t num_blocks, int block_size, int num_kv_heads, int head_dim, int dtype,
                    void *stream) {

@@ -44,6 +44,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
+#include "tma_maps.cuh"
 
 namespace pa {
 namespace {
@@ -484,7 +485,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             }
             auto accumulate = [&](uint32_t j) -> bool {
                 const int buf = j & 1;
-                if (!mbar_wait(&bars.o_full[buf], (j >> 1) & 1)) return false;
+                if (!warp_wait(&bars.o_full[buf], (j >> 1) & 1)) return false;
                 tc_fence_after();
                 float o[16];
                 tmem_ld16(tmem + lane_off + 2 * kN + buf * kN, o);
@@ -497,7 +498,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             };
             for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
                 const int buf = it & 1, stage = it % kStages;
-                if (*abort_flag || !mbar_wait(&bars.s_full[buf], (it >> 1) & 1)) {
+                if (__any_sync(0xffffffffu, *abort_flag != 0) || !warp_wait(&bars.s_full[buf], (it >> 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -518,7 +519,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                     if (lane == 0) rd[q4 * kN + g] = mx;
                 }
                 mbar_arrive(&bars.red[it & 1]);
-                if (!mbar_wait(&bars.red[it & 1], (it >> 1) & 1)) {
+                if (!warp_wait(&bars.red[it & 1], (it >> 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -537,12 +538,13 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                     unsigned char *dst = pb + g * 128 + ((((colb >> 4) ^ (g & 7)) << 4) | (colb & 15));
                     *reinterpret_cast<uint16_t *>(dst) = bits;
                 }
+                // masked token: its V row may hold anything (NaN included) and P = 0,
+                // so zero the row once the stage's copies have landed
+                if (__any_sync(0xffffffffu, !valid) && !warp_wait(&bars.full[stage], (it / kStages) & 1)) {
+                    ok = false;
+                    break;
+                }
                 if (!valid) {
-                    // masked token: its V row may hold anything (NaN included) and P = 0
-                    if (!mbar_wait(&bars.full[stage], (it / kStages) & 1)) {
-                        ok = false;
-                        break;
-                    }
                     uint4 *v0 = reinterpret_cast<uint4 *>(sV + stage * kKVBytes + row * 128);
                     uint4 *v1 = reinterpret_cast<uint4 *>(sV + stage * kKVBytes + kChunkBytes + row * 128);
 #pragma unroll
@@ -573,7 +575,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                 if (lane == 0) lred[q4 * kN + g] = ls;
             }
             mbar_arrive(bars.fin);
-            if (!mbar_wait(bars.fin, nfin++ & 1)) {
+            if (!warp_wait(bars.fin, nfin++ & 1)) {
                 ok = false;
                 break;
             }
@@ -581,7 +583,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
 #pragma unroll
             for (int g = 0; g < GT; ++g) l_tot[g] = lred[g] + lred[kN + g] + lred[2 * kN + g] + lred[3 * kN + g];
             mbar_arrive(bars.fin);                    // lred may be rewritten after this phase
-            if (!mbar_wait(bars.fin, nfin++ & 1)) {
+            if (!warp_wait(bars.fin, nfin++ & 1)) {
                 ok = false;
                 break;
             }
@@ -621,37 +623,12 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
 
 // ---- host side -----------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
 bool make_cache_map(CUtensorMap *m, const void *base, const DecodeParams &p, CUtensorMapDataType dt) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t es = 2;
-    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)p.num_kv_heads, (cuuint64_t)p.block_size,
-                          (cuuint64_t)p.num_blocks};
-    cuuint64_t strides[3] = {kD * es, (cuuint64_t)p.num_kv_heads * kD * es,
-                             (cuuint64_t)p.block_size * p.num_kv_heads * kD * es};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)p.block_size, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return make_kv_cache_map(m, base, p.num_blocks, p.block_size, p.num_kv_heads, dt);
 }
 
 bool make_q_map(CUtensorMap *m, const DecodeParams &p, CUtensorMapDataType dt) {
-    auto enc = encode_fn();
+    auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.num_seqs * p.num_heads};
     cuuint64_t strides[1] = {kD * 2};

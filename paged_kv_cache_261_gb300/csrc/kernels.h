@@ -34,6 +34,37 @@ struct DecodeParams {
     float scale_log2;          // scale * log2(e)
 };
 
+// Chunked prefill: every query row of a packed chunk attends causally.
+struct PrefillParams {
+    void *out;                  // [num_query_tokens, num_heads, head_dim]
+    const void *q;              // same layout
+    const void *key_cache;
+    const void *value_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    const int32_t *query_start_loc;   // [num_seqs + 1]
+    unsigned int *err;
+    int64_t num_blocks;
+    int64_t num_query_tokens;
+    int max_blocks_per_seq;
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int group;                  // num_heads / num_kv_heads
+    int group_pad;              // group rounded up to a power of two
+    int rows_q;                 // query tokens per item: 128 / group_pad
+    int qtiles;                 // ceil(max_query_len / rows_q)
+    int head_dim;
+    int block_size;
+    int log2_block_size;
+    int max_query_len;
+    int context_limit;          // max_blocks_per_seq * block_size
+    float scale_log2;
+};
+
+bool prefill_tc_supported(const PrefillParams &p, int dtype);
+int launch_prefill_tc(const PrefillParams &p, int dtype, cudaStream_t stream);
+
 int launch_kv_write(const void *k, const void *v, const int32_t *slot_mapping, int64_t num_tokens,
                     void *key_cache, void *value_cache, int64_t num_slots, int row_bytes,
                     unsigned int *err, cudaStream_t stream);

@@ -1,0 +1,501 @@
+// Chunked-prefill attention over the paged cache on the sm_100 tensor cores.
+//
+// The paged step of "CS349E lecture 7: 01_paged_attention.py" (demo 1, demo 2)
+// writes a chunk's K/V into its blocks and then lets every position of the
+// chunk attend; "04 - Paged Attention 实现进度" B.2/D.2 packs the chunks of a
+// batch with cu_seqlens_q (query_start_loc). Query row i of sequence b sits at
+// position ctx_b - q_len_b + i and attends to positions 0..pos (causal), each
+// query head h reading kv head h / G. For every (row, head) the result is one
+// softmax over its visible keys, taken online here: a running max and sum per
+// row, with the accumulated output rescaled when the max grows.
+//
+// Work item = (sequence, kv head, tile of query tokens). The item's 128 MMA
+// rows are (query token, head of the group) pairs: QT = 128 / Gp tokens x Gp
+// heads, Gp = G rounded up to a power of two. Per tile of 128 keys:
+//   S[128 rows x 128 keys] = Q . K^T    (tcgen05 kind::f16, M=128 N=128 K=128)
+//   O[128 rows x 128 dims] += P . V     (P from shared memory, V MN-major)
+// S is double-buffered and O stays in tensor memory (384 of 512 columns).
+// Thread = row for the softmax, so the max and the sum are thread-local; O is
+// rescaled (tcgen05.ld / st of the row) only when a row's max grows by more than
+// 2^8, otherwise the stale reference max is kept (the final O / l is the same).
+//
+// Roles (192 threads, one persistent CTA per SM):
+//   warp 0     TMA: the item's query rows (3-D map over [tokens, heads, dims]),
+//              then per key tile the K/V boxes of each physical block through
+//              the block table into a 2-stage ring; blocks past the last visible
+//              key load from an out-of-range coordinate (zeros).
+//   warp 1     one thread issues the MMAs and owns tensor memory.
+//   warps 2-5  softmax (scale, causal mask, exp2, P to shared memory, V rows of
+//              keys past the last visible one zeroed) and the epilogue O / l.
+// Items are ordered with the query tiles of one (sequence, kv head) adjacent,
+// so the CTAs working on them at the same time share its K/V through L2.
+// Every wait is bounded; on a timeout the kernel sets PA_DEVERR_WAIT and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+#include "tma_maps.cuh"
+
+namespace pa {
+namespace {
+
+using namespace sm100;
+
+constexpr int kD = 128;
+constexpr int kKT = 128;                       // keys per tile
+constexpr int kRows = 128;                     // MMA rows per item
+constexpr int kStages = 2;
+constexpr int kChunk = 128 * 128;              // 128 rows x 128 bytes (one 64-element half)
+constexpr int kKVBytes = 2 * kChunk;           // one K (or V) tile
+constexpr int kQBytes = 2 * kChunk;
+constexpr int kPBytes = 2 * kChunk;
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr uint32_t kTmemCols = 512;            // S[2] x 128 + O x 128 (+ spare)
+constexpr uint32_t kColO = 2 * kKT;
+constexpr float kRescaleLog2 = 8.f;            // keep the reference max until a row's max grows by 2^8
+
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kStages * kKVBytes;
+constexpr int kOffQ = kOffV + kStages * kKVBytes;
+constexpr int kOffP = kOffQ + kQBytes;
+constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kNumBars = 17;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemUsed = kOffMisc + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct PItem {
+    int b, kvh, q_row0, nq, pos_first, kmax, ntiles;
+};
+
+// Item idx -> (sequence, kv head, query tile); false when the tile is empty or
+// the sequence's lengths are inconsistent (reported once, by query tile 0).
+__device__ __forceinline__ bool get_pitem(int idx, const PrefillParams &p, PItem &it) {
+    const int qt = idx % p.qtiles;
+    const int rest = idx / p.qtiles;
+    it.kvh = rest % p.num_kv_heads;
+    it.b = rest / p.num_kv_heads;
+    const int q_start = p.query_start_loc[it.b];
+    const int q_len = p.query_start_loc[it.b + 1] - q_start;
+    const int ctx = p.context_lens[it.b];
+    if (q_len < 0 || q_len > p.max_query_len || ctx < q_len || ctx > p.context_limit || q_start < 0 ||
+        (int64_t)q_start + q_len > p.num_query_tokens) {
+        if (qt == 0 && it.kvh == 0) raise_error(p.err, PA_DEVERR_CONTEXT);
+        return false;
+    }
+    const int qi0 = qt * p.rows_q;
+    if (qi0 >= q_len) return false;
+    it.q_row0 = q_start + qi0;
+    it.nq = min(p.rows_q, q_len - qi0);
+    it.pos_first = ctx - q_len + qi0;
+    it.kmax = it.pos_first + it.nq;              // keys 0 .. kmax-1 are visible to some row
+    it.ntiles = (it.kmax + kKT - 1) / kKT;
+    return true;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&v);
+    } else {
+        const __half2 v = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&v);
+    }
+}
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    } else {
+        const __half2 h = *reinterpret_cast<const __half2 *>(&u);
+        return __half22float2(h);
+    }
+}
+
+template <typename T>
+__global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                 const __grid_constant__ CUtensorMap tm_v,
+                                                                 const __grid_constant__ CUtensorMap tm_q,
+                                                                 const PrefillParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *sK = smem + kOffK;
+    unsigned char *sV = smem + kOffV;
+    unsigned char *sQ = smem + kOffQ;
+    unsigned char *sP = smem + kOffP;
+    uint64_t *bb = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *full = bb, *empty = bb + 2, *s_full = bb + 4, *s_free = bb + 6, *p_full = bb + 8, *o_done = bb + 10;
+    uint64_t *q_full = bb + 12, *q_empty = bb + 13, *o_free = bb + 14;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = p.group, Gp = p.group_pad;
+    const int total_items = p.num_seqs * p.num_kv_heads * p.qtiles;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        mbar_init(o_free, 4);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        const int nbt = kKT / p.block_size;
+        uint32_t it = 0, n = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+            PItem I;
+            if (!get_pitem(idx, p, I)) continue;
+            const int32_t *table = p.block_tables + (int64_t)I.b * p.max_blocks_per_seq;
+            int w = 1;
+            if (lane == 0) {
+                w = mbar_wait(q_empty, (n & 1) ^ 1) ? 1 : 0;
+                if (w) {
+                    mbar_arrive_expect_tx(q_full, kQBytes);
+                    tma_load_3d(sQ, &tm_q, q_full, 0, I.kvh * G, I.q_row0);
+                    tma_load_3d(sQ + kChunk, &tm_q, q_full, 64, I.kvh * G, I.q_row0);
+                }
+            }
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (!w) {
+                ok = false;
+                break;
+            }
+            ++n;
+            for (int j = 0; j < I.ntiles; ++j, ++it) {
+                const int stage = it & 1;
+                int phys = (int)p.num_blocks;
+                if (lane < nbt) {
+                    const int tok = j * kKT + lane * p.block_size;
+                    if (tok < I.kmax) {
+                        const int e = table[tok >> p.log2_block_size];
+                        if (e >= 0 && e < p.num_blocks) phys = e;
+                        else raise_error(p.err, PA_DEVERR_BLOCK_ID);
+                    }
+                }
+                if (lane == 0) w = mbar_wait(&empty[stage], ((it >> 1) & 1) ^ 1) ? 1 : 0;
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&full[stage], 2 * kKVBytes);
+                __syncwarp();
+                if (lane < nbt) {
+                    unsigned char *dk = sK + stage * kKVBytes + lane * p.block_size * 128;
+                    unsigned char *dv = sV + stage * kKVBytes + lane * p.block_size * 128;
+                    tma_load_4d(dk, &tm_k, &full[stage], 0, I.kvh, 0, phys);
+                    tma_load_4d(dk + kChunk, &tm_k, &full[stage], 64, I.kvh, 0, phys);
+                    tma_load_4d(dv, &tm_v, &full[stage], 0, I.kvh, 0, phys);
+                    tma_load_4d(dv + kChunk, &tm_v, &full[stage], 64, I.kvh, 0, phys);
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            raise_error(p.err, PA_DEVERR_WAIT);
+        }
+        if (lane == 0) {   // drain copies in flight
+            const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
+            for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j & 1], (j >> 1) & 1);
+            if (n > 0) mbar_wait(q_full, (n - 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+            const uint32_t idesc_s = instr_desc_f16(kRows, kKT, kBf16, false, false);
+            const uint32_t idesc_o = instr_desc_f16(kRows, kD, kBf16, false, true);
+            const uint32_t sK0 = smem_addr(sK), sV0 = smem_addr(sV), sQ0 = smem_addr(sQ), sP0 = smem_addr(sP);
+            uint32_t it = 0, n = 0;
+            bool ok = true;
+            // O += P(j) V(j); `first` starts the item's accumulator
+            auto issue_pv = [&](uint32_t j, bool first) -> bool {
+                if (first && n > 1 && !mbar_wait(o_free, (n - 2) & 1)) return false;
+                if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t vb = sV0 + (j & 1) * kKVBytes, pb = sP0 + (j & 1) * kPBytes;
+#pragma unroll
+                for (int kk = 0; kk < kKT / 16; ++kk) {
+                    const uint64_t a = smem_desc(pb + (kk >> 2) * kChunk + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc(vb + kk * 2048, kChunk, 1024);
+                    mma_f16(tmem + kColO, a, b, idesc_o, (first && kk == 0) ? 0u : 1u);
+                }
+                mma_commit(&o_done[j & 1]);
+                mma_commit(&empty[j & 1]);
+                return true;
+            };
+            for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+                PItem I;
+                if (!get_pitem(idx, p, I)) continue;
+                if (!mbar_wait(q_full, n & 1)) {
+                    ok = false;
+                    break;
+                }
+                ++n;
+                for (int j = 0; j < I.ntiles; ++j, ++it) {
+                    const int stage = it & 1;
+                    if (*abort_flag || !mbar_wait(&full[stage], (it >> 1) & 1) ||
+                        !mbar_wait(&s_free[stage], ((it >> 1) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kb = sK0 + stage * kKVBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+                        mma_f16(tmem + stage * kKT, smem_desc(sQ0 + off, 16, 1024), smem_desc(kb + off, 16, 1024),
+                                idesc_s, kk > 0);
+                    }
+                    mma_commit(&s_full[stage]);
+                    if (j == I.ntiles - 1) mma_commit(q_empty);
+                    if (j > 0 && !issue_pv(it - 1, j == 1)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!ok) break;
+                if (!issue_pv(it - 1, I.ntiles == 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                raise_error(p.err, PA_DEVERR_WAIT);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;                 // MMA row of this thread (and key row for V zeroing)
+        const int gshift = 31 - __clz(Gp);
+        const int qi = r >> gshift, g = r & (Gp - 1);
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        T *out = reinterpret_cast<T *>(p.out);
+        uint32_t it = 0, n = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+            PItem I;
+            if (!get_pitem(idx, p, I)) continue;
+            const bool row_valid = qi < I.nq && g < G;
+            const int pos = row_valid ? I.pos_first + qi : -1;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < I.ntiles; ++j, ++it) {
+                const int buf = it & 1;
+                if (__any_sync(0xffffffffu, *abort_flag != 0) || !warp_wait(&s_full[buf], (it >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t sr[kKT];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + buf * kKT + c * 32, sr + c * 32);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free[buf]);
+
+                const int k0 = j * kKT;
+                float m_tile = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kKT; ++c) {
+                    const float v = (k0 + c <= pos) ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
+                    sr[c] = __float_as_uint(v);
+                    m_tile = fmaxf(m_tile, v);
+                }
+                const bool grow = m_tile > m_ref + kRescaleLog2;
+                const float alpha = grow ? fast_exp2(m_ref - m_tile) : 1.f;
+                if (grow) m_ref = m_tile;
+                l *= alpha;
+                if (__any_sync(0xffffffffu, grow && j > 0)) {
+                    // O holds tiles up to j-1: rescale it once their MMA has finished
+                    const uint32_t pj = it - 1;
+                    if (!warp_wait(&o_done[pj & 1], (pj >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tmem + lane_off + kColO + c * 32, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tmem + lane_off + kColO + c * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+                // P buffer `buf` was last read by the MMA of tile it-2
+                if (it >= 2 && !warp_wait(&o_done[buf], ((it - 2) >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char *prow = sP + buf * kPBytes + r * 128;
+#pragma unroll
+                for (int u = 0; u < kKT / 8; ++u) {
+                    float pv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float sv = __uint_as_float(sr[u * 8 + e]);
+                        pv[e] = sv == -INFINITY ? 0.f : fast_exp2(sv - m_ref);
+                    }
+                    uint4 pk;
+                    pk.x = pack2<T>(pv[0], pv[1]);
+                    pk.y = pack2<T>(pv[2], pv[3]);
+                    pk.z = pack2<T>(pv[4], pv[5]);
+                    pk.w = pack2<T>(pv[6], pv[7]);
+                    const float2 a0 = unpack2<T>(pk.x), a1 = unpack2<T>(pk.y);
+                    const float2 a2 = unpack2<T>(pk.z), a3 = unpack2<T>(pk.w);
+                    l += (a0.x + a0.y) + (a1.x + a1.y) + (a2.x + a2.y) + (a3.x + a3.y);
+                    const int chunk = u >> 3, unit = (u & 7) ^ (r & 7);
+                    *reinterpret_cast<uint4 *>(prow + chunk * kChunk + unit * 16) = pk;
+                }
+                // key row r past every row's last visible key: its slot may hold anything
+                const bool zero_v = k0 + r >= I.kmax;
+                if (__any_sync(0xffffffffu, zero_v) && !warp_wait(&full[buf], (it >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (zero_v) {
+                    uint4 *v0 = reinterpret_cast<uint4 *>(sV + buf * kKVBytes + r * 128);
+                    uint4 *v1 = reinterpret_cast<uint4 *>(sV + buf * kKVBytes + kChunk + r * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        v0[c] = make_uint4(0, 0, 0, 0);
+                        v1[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[buf]);
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l of this item's rows
+            const uint32_t last = it - 1;
+            if (!warp_wait(&o_done[last & 1], (last >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float inv = row_valid ? 1.f / l : 0.f;
+            T *orow = out + ((int64_t)(I.q_row0 + qi) * p.num_heads + I.kvh * G + g) * kD;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + kColO + c * 32, o);
+                if (row_valid) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 pk;
+                        pk.x = pack2<T>(__uint_as_float(o[u * 8 + 0]) * inv, __uint_as_float(o[u * 8 + 1]) * inv);
+                        pk.y = pack2<T>(__uint_as_float(o[u * 8 + 2]) * inv, __uint_as_float(o[u * 8 + 3]) * inv);
+                        pk.z = pack2<T>(__uint_as_float(o[u * 8 + 4]) * inv, __uint_as_float(o[u * 8 + 5]) * inv);
+                        pk.w = pack2<T>(__uint_as_float(o[u * 8 + 6]) * inv, __uint_as_float(o[u * 8 + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + c * 32 + u * 8) = pk;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);
+            ++n;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            raise_error(p.err, PA_DEVERR_WAIT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <typename T>
+int launch_prefill_t(const PrefillParams &p, CUtensorMapDataType dt, cudaStream_t stream) {
+    auto kern = prefill_tc_kernel<T>;
+    static bool attr_set[kMaxDevices] = {};
+    static int num_sms[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+            return -1;
+        if (cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        attr_set[dev] = true;
+    }
+    CUtensorMap mk, mv, mq;
+    if (!make_kv_cache_map(&mk, p.key_cache, p.num_blocks, p.block_size, p.num_kv_heads, dt) ||
+        !make_kv_cache_map(&mv, p.value_cache, p.num_blocks, p.block_size, p.num_kv_heads, dt))
+        return -1;
+    // queries as [tokens, heads, dims]; one box = 64 dims x Gp heads x QT tokens (128 rows)
+    auto enc = tensor_map_encoder();
+    if (!enc) return -1;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.num_heads, (cuuint64_t)p.num_query_tokens};
+    cuuint64_t strides[2] = {kD * 2, (cuuint64_t)p.num_heads * kD * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.group_pad, (cuuint32_t)p.rows_q};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&mq, dt, 3, const_cast<void *>(p.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return -1;
+    const int64_t items = (int64_t)p.num_seqs * p.num_kv_heads * p.qtiles;
+    const int grid = (int)(items < num_sms[dev] ? items : num_sms[dev]);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, mq, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PrefillParams &p, int dtype) {
+    return (dtype == PA_DTYPE_BF16 || dtype == PA_DTYPE_F16) && p.head_dim == kD && p.group >= 1 &&
+           p.group <= 16 && p.block_size >= 8 && p.block_size <= kKT && p.num_blocks < INT32_MAX &&
+           p.num_query_tokens < INT32_MAX && (int64_t)p.num_seqs * p.num_kv_heads * p.qtiles < INT32_MAX;
+}
+
+int launch_prefill_tc(const PrefillParams &p, int dtype, cudaStream_t stream) {
+    if (!prefill_tc_supported(p, dtype)) return -2;
+    if (dtype == PA_DTYPE_BF16) return launch_prefill_t<__nv_bfloat16>(p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, stream);
+    return launch_prefill_t<__half>(p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, stream);
+}
+
+}  // namespace pa

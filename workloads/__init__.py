@@ -602,3 +602,23 @@ def chunked_prefill(seed: int = 1006, num_seqs: int = 16, chunk: int = 512,
     rng = np.random.default_rng(seed)
     prior = rng.integers(0, 3585, size=num_seqs)
     return make_prefill("chunked_prefill", seed, prior, np.full(num_seqs, chunk), 32, 8, 128, 16, dtype)
+
+
+def fill_prior_torch(pw: PrefillWorkload, key_cache, value_cache, chunk_tokens: int = 1 << 16):
+    """Write every sequence's cached tokens before its chunk (positions < ctx - q_len)."""
+    import torch
+    w = pw.base
+    prior = (w.context_lens - pw.q_lens).astype(np.int64)
+    seq_idx = np.repeat(np.arange(w.num_seqs, dtype=np.int64), prior)
+    starts = np.repeat(np.cumsum(prior) - prior, prior)
+    pos = np.arange(int(prior.sum()), dtype=np.int64) - starts
+    slots = w._slots(seq_idx, pos) if seq_idx.size else np.zeros(0, np.int64)
+    kflat = key_cache.view(-1, w.row_elems)
+    vflat = value_cache.view(-1, w.row_elems)
+    dev = key_cache.device
+    for s in range(0, seq_idx.shape[0], chunk_tokens):
+        si = torch.as_tensor(seq_idx[s:s + chunk_tokens], device=dev)
+        pi = torch.as_tensor(pos[s:s + chunk_tokens], device=dev)
+        sl = torch.as_tensor(slots[s:s + chunk_tokens], device=dev)
+        kflat[sl] = w.kv_rows(TID_K, si, pi).to(key_cache.dtype)
+        vflat[sl] = w.kv_rows(TID_V, si, pi).to(value_cache.dtype)
