@@ -163,8 +163,8 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
  * PA_DEVERR_BLOCK_ID and reads as zeros.
  *
  * Supported: dtype f16/bf16, head_dim 128, num_heads/num_kv_heads <= 16,
- * block_size a power of two in [8, 128]; else PA_ERR_UNSUPPORTED.
- * Allocates nothing.
+ * block_size a power of two in [8, 128]; else PA_ERR_UNSUPPORTED. scale must
+ * be positive (PA_ERR_INVALID_ARG otherwise). Allocates nothing.
  */
 int pa_paged_attention_prefill(void *out, const void *q, const void *key_cache,
                                const void *value_cache, const int32_t *block_tables,

@@ -226,7 +226,7 @@ int pa_paged_attention_prefill(void *out, const void *q, const void *key_cache, 
         return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
         return PA_ERR_INVALID_ARG;
-    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+    if (!(scale > 0.f)) return PA_ERR_INVALID_ARG;     // the kernel takes the max of unscaled scores
     const int64_t table_cap = (int64_t)max_blocks_per_seq * block_size;
     if (table_cap > INT32_MAX || num_query_tokens > INT32_MAX) return PA_ERR_UNSUPPORTED;
     pa::PrefillParams p{};

@@ -323,20 +323,31 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                 }
                 tc_fence_after();
                 uint32_t sr[kKT];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + buf * kKT + c * 32, sr + c * 32);
+                tmem_ld64(tmem + lane_off + buf * kKT, sr);
+                tmem_ld64(tmem + lane_off + buf * kKT + 64, sr + 64);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_free[buf]);
 
+                // Raw scores; the scale (> 0) is folded into the exponent below. Only tiles
+                // reaching past the item's first position need the causal mask.
                 const int k0 = j * kKT;
-                float m_tile = -INFINITY;
+                if (k0 + kKT - 1 > I.pos_first) {
 #pragma unroll
-                for (int c = 0; c < kKT; ++c) {
-                    const float v = (k0 + c <= pos) ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-                    sr[c] = __float_as_uint(v);
-                    m_tile = fmaxf(m_tile, v);
+                    for (int c = 0; c < kKT; ++c)
+                        if (k0 + c > pos) sr[c] = __float_as_uint(-INFINITY);
                 }
+                float mx[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sr[e]);
+#pragma unroll
+                for (int c = 8; c < kKT; c += 8) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], __uint_as_float(sr[c + e]));
+                }
+                const float m_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float m_tile = m_raw * p.scale_log2;
                 const bool grow = m_tile > m_ref + kRescaleLog2;
                 const float alpha = grow ? fast_exp2(m_ref - m_tile) : 1.f;
                 if (grow) m_ref = m_tile;
@@ -365,14 +376,13 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                     break;
                 }
                 unsigned char *prow = sP + buf * kPBytes + r * 128;
+                const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;    // rows with no visible key: p = 0
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int u = 0; u < kKT / 8; ++u) {
                     float pv[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float sv = __uint_as_float(sr[u * 8 + e]);
-                        pv[e] = sv == -INFINITY ? 0.f : fast_exp2(sv - m_ref);
-                    }
+                    for (int e = 0; e < 8; ++e) pv[e] = fast_exp2(fmaf(__uint_as_float(sr[u * 8 + e]), p.scale_log2, neg_m));
                     uint4 pk;
                     pk.x = pack2<T>(pv[0], pv[1]);
                     pk.y = pack2<T>(pv[2], pv[3]);
@@ -380,10 +390,14 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                     pk.w = pack2<T>(pv[6], pv[7]);
                     const float2 a0 = unpack2<T>(pk.x), a1 = unpack2<T>(pk.y);
                     const float2 a2 = unpack2<T>(pk.z), a3 = unpack2<T>(pk.w);
-                    l += (a0.x + a0.y) + (a1.x + a1.y) + (a2.x + a2.y) + (a3.x + a3.y);
+                    ls[0] += a0.x + a0.y;
+                    ls[1] += a1.x + a1.y;
+                    ls[2] += a2.x + a2.y;
+                    ls[3] += a3.x + a3.y;
                     const int chunk = u >> 3, unit = (u & 7) ^ (r & 7);
                     *reinterpret_cast<uint4 *>(prow + chunk * kChunk + unit * 16) = pk;
                 }
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 // key row r past every row's last visible key: its slot may hold anything
                 const bool zero_v = k0 + r >= I.kmax;
                 if (__any_sync(0xffffffffu, zero_v) && !warp_wait(&full[buf], (it >> 1) & 1)) {
@@ -415,18 +429,18 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
             const float inv = row_valid ? 1.f / l : 0.f;
             T *orow = out + ((int64_t)(I.q_row0 + qi) * p.num_heads + I.kvh * G + g) * kD;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + kColO + c * 32, o);
+            for (int c = 0; c < 2; ++c) {
+                uint32_t o[64];
+                tmem_ld64(tmem + lane_off + kColO + c * 64, o);
                 if (row_valid) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < 8; ++u) {
                         uint4 pk;
                         pk.x = pack2<T>(__uint_as_float(o[u * 8 + 0]) * inv, __uint_as_float(o[u * 8 + 1]) * inv);
                         pk.y = pack2<T>(__uint_as_float(o[u * 8 + 2]) * inv, __uint_as_float(o[u * 8 + 3]) * inv);
                         pk.z = pack2<T>(__uint_as_float(o[u * 8 + 4]) * inv, __uint_as_float(o[u * 8 + 5]) * inv);
                         pk.w = pack2<T>(__uint_as_float(o[u * 8 + 6]) * inv, __uint_as_float(o[u * 8 + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + c * 32 + u * 8) = pk;
+                        *reinterpret_cast<uint4 *>(orow + c * 64 + u * 8) = pk;
                     }
                 }
             }
