@@ -192,6 +192,19 @@ class Step:
         self.ws = torch.empty(max(pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim,
                                                             self.max_ctx, 0), 16),
                               dtype=torch.uint8, device=device)
+        self.shared = None
+        self.unique_kv_bytes = None
+        if name == "shared_prefix":
+            # each prompt's shared blocks are read once for its 8 samples
+            pl, gm = pa.prefix_groups(w.block_tables, w.context_lens, w.block_size, max_members=8)
+            self.shared = (torch.as_tensor(pl, device=device), torch.as_tensor(gm, device=device),
+                           int(pl.max()) if pl.size else 0)
+            self.ws = torch.empty(pa.decode_shared_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim,
+                                                                   self.max_ctx, 0), dtype=torch.uint8,
+                                  device=device)
+            lead_prefix = sum(int(pl[row[0]]) for row in gm)
+            uniq_tokens = int((w.context_lens.astype(np.int64) - pl).sum()) + lead_prefix
+            self.unique_kv_bytes = uniq_tokens * w.row_elems * 2 * 2
         es = {"f32": 4, "f16": 2, "bf16": 2}[w.dtype]
         ab = w.algorithmic_bytes()
         self.decode_bytes = ab["decode"]
@@ -200,6 +213,8 @@ class Step:
         self.step_bytes = self.decode_bytes + self.write_bytes + self.copy_bytes
         self.launches_per_step = 1 + (1 if self.copy_pairs is not None else 0) + 1 + (
             1 if pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, self.max_ctx, 0) else 0)
+        if self.shared is not None:
+            self.launches_per_step = 1 + 1 + 3     # copy, write, shared pass + private pass + merge
         torch.cuda.synchronize()
 
     def _shared_prefix_state(self):
@@ -237,8 +252,14 @@ class Step:
         pa.paged_kv_write(self.k_new, self.v_new, self.slots, self.kc, self.vc)
         if ev is not None:
             ev[0].record()
-        pa.paged_attention_decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl, self.w.scale,
-                                  max_context_len=self.max_ctx, workspace=self.ws)
+        if self.shared is not None:
+            pl, gm, mp = self.shared
+            pa.paged_attention_decode_shared(self.out, self.q, self.kc, self.vc, self.bt, self.cl, pl, gm,
+                                             self.w.scale, max_context_len=self.max_ctx, max_prefix_len=mp,
+                                             workspace=self.ws)
+        else:
+            pa.paged_attention_decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl, self.w.scale,
+                                      max_context_len=self.max_ctx, workspace=self.ws)
         if ev is not None:
             ev[1].record()
 
@@ -251,6 +272,8 @@ class Step:
                 "written_tokens": int(self.slots.shape[0]),
                 "copied_blocks": 0 if self.copy_pairs is None else int(self.copy_pairs.shape[0]),
                 "partition_size": 512,
+                "shared_prefix_decode": self.shared is not None,
+                "unique_kv_bytes": self.unique_kv_bytes,
                 "decode_kernel": os.environ.get("PA_DECODE_KERNEL", "auto"),
                 "l2": f"inputs larger than L2: {w.algorithmic_bytes()['kv'] / 1e9:.2f} GB of K/V read per step "
                       f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"}
@@ -542,8 +565,10 @@ def run_e2e(st: Step, args, device):
     device -> host copy of the output."""
     import torch
     n = max(min(args.steps, 500), 10)
-    host = {k: t.cpu().pin_memory() for k, t in
-            (("q", st.q), ("k", st.k_new), ("v", st.v_new), ("slots", st.slots), ("bt", st.bt), ("cl", st.cl))}
+    items = [("q", st.q), ("k", st.k_new), ("v", st.v_new), ("slots", st.slots), ("bt", st.bt), ("cl", st.cl)]
+    if st.shared is not None:
+        items += [("pl", st.shared[0]), ("gm", st.shared[1])]
+    host = {k: t.cpu().pin_memory() for k, t in items}
     out_h = torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
@@ -556,8 +581,13 @@ def run_e2e(st: Step, args, device):
         if st.copy_pairs is not None:
             pa.copy_blocks(st.kc, st.vc, st.copy_pairs)
         pa.paged_kv_write(dev_in["k"], dev_in["v"], dev_in["slots"], st.kc, st.vc)
-        pa.paged_attention_decode(st.out, dev_in["q"], st.kc, st.vc, dev_in["bt"], dev_in["cl"], st.w.scale,
-                                  max_context_len=st.max_ctx, workspace=st.ws)
+        if st.shared is not None:
+            pa.paged_attention_decode_shared(st.out, dev_in["q"], st.kc, st.vc, dev_in["bt"], dev_in["cl"],
+                                             dev_in["pl"], dev_in["gm"], st.w.scale, max_context_len=st.max_ctx,
+                                             max_prefix_len=st.shared[2], workspace=st.ws)
+        else:
+            pa.paged_attention_decode(st.out, dev_in["q"], st.kc, st.vc, dev_in["bt"], dev_in["cl"], st.w.scale,
+                                      max_context_len=st.max_ctx, workspace=st.ws)
         out_h.copy_(st.out, non_blocking=True)
 
     for _ in range(3):

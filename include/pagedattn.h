@@ -141,6 +141,43 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
                               size_t workspace_bytes, int dtype, void *stream);
 
 /*
+ * Decode attention that reads each shared prefix once for all sequences that
+ * share it.
+ * [P2 demo 3: forked samples share the prompt's blocks by reference count;
+ *  P3 A.1/B.1: several block tables may point at the same physical blocks
+ *  (prefix sharing)]
+ *
+ * Same result as pa_paged_attention_decode. group_members[g, 0..max_members)
+ * lists the sequences of group g (-1 = empty slot, members first); a sequence
+ * belongs to at most one group. prefix_lens[b] is the number of leading tokens
+ * sequence b shares with its group (0 outside groups); all members of a group
+ * must have the same prefix_lens and identical block-table entries for those
+ * tokens (pa_prefix_groups derives such groups from the tables). The shared
+ * tokens of a group are read once, through the first member's table, for all
+ * members' queries together; each sequence's remaining tokens are read as in
+ * pa_paged_attention_decode; the split-K merge combines both. max_prefix_len
+ * is a host-side bound on prefix_lens. max_members * G' <= 128 (G' = group size
+ * num_heads/num_kv_heads rounded up to a power of two).
+ *
+ * Supported: dtype f16/bf16, head_dim 128, num_heads/num_kv_heads <= 16,
+ * block_size a power of two in [8, 128], scale > 0. workspace >=
+ * pa_decode_shared_workspace_bytes(...) bytes (NULL: taken with cudaMallocAsync
+ * on the stream and released after the merge).
+ */
+size_t pa_decode_shared_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                        int max_context_len, int partition_size);
+
+int pa_paged_attention_decode_shared(void *out, const void *q, const void *key_cache,
+                                     const void *value_cache, const int32_t *block_tables,
+                                     int max_blocks_per_seq, const int32_t *context_lens,
+                                     const int32_t *prefix_lens, const int32_t *group_members,
+                                     int num_groups, int max_members, int max_prefix_len,
+                                     int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int64_t num_blocks, float scale,
+                                     int max_context_len, int partition_size, void *workspace,
+                                     size_t workspace_bytes, int dtype, void *stream);
+
+/*
  * Chunked-prefill attention over the paged cache.
  * [P2 demo 1 and demo 2: a paged step writes the chunk's K/V into its blocks,
  *  then every position of the chunk attends to the positions up to its own;
@@ -293,6 +330,20 @@ int pa_alloc_export(const pa_allocator *a, const int64_t *seq_ids, int64_t n_seq
 /* Raw pool operations (take one block with count 1; drop one reference). */
 int pa_alloc_block(pa_allocator *a, int32_t *block_out);
 int pa_alloc_decref(pa_allocator *a, int32_t block);
+
+/*
+ * Host helper: group sequences whose block tables start with the same physical
+ * blocks (the prefix sharing that fork() creates). Candidates need at least
+ * min_shared_blocks full blocks and are keyed by their first block; each group
+ * of 2..max_members sequences (larger sets are split in order) gets the longest
+ * run of leading blocks that all members hold identically and completely.
+ * Outputs prefix_lens[num_seqs] (shared tokens, 0 outside groups),
+ * group_members[num_seqs * max_members] (num_groups rows used, -1 padded).
+ * Host memory only.
+ */
+int pa_prefix_groups(const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                     int max_blocks_per_seq, int block_size, int max_members, int min_shared_blocks,
+                     int32_t *prefix_lens, int32_t *group_members, int *num_groups);
 
 /* Reference count of one block. */
 int pa_alloc_refcount(const pa_allocator *a, int32_t block, int32_t *count);

@@ -12,6 +12,9 @@ Entry points (same names as the C ABI, without the ``pa_`` prefix):
                          context_lens, scale, block_size, num_kv_heads)
   paged_attention_prefill(out, q, key_cache, value_cache, block_tables,
                           context_lens, query_start_loc, scale, max_query_len)
+  paged_attention_decode_shared(out, q, key_cache, value_cache, block_tables,
+                                context_lens, prefix_lens, group_members, scale)
+  prefix_groups(block_tables, context_lens, block_size)   (host)
   copy_blocks(key_cache, value_cache, src_dst_pairs)
   get_device_error()
   BlockAllocator: the host block manager (free list, reference counts, fork,
@@ -71,6 +74,10 @@ _decl("pa_paged_attention_decode", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i
                                     _i64, _f, _i32, _i32, _vp, _sz, _i32, _vp])
 _decl("pa_copy_blocks", [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp])
 _decl("pa_get_device_error", [_vp, ctypes.POINTER(ctypes.c_uint32)])
+_decl("pa_decode_shared_workspace_bytes", [_i32, _i32, _i32, _i32, _i32], _sz)
+_decl("pa_paged_attention_decode_shared", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                           _i32, _i32, _i32, _i32, _i64, _f, _i32, _i32, _vp, _sz, _i32, _vp])
+_decl("pa_prefix_groups", [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, ctypes.POINTER(ctypes.c_int)])
 _decl("pa_paged_attention_prefill", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
                                      _i32, _i64, _f, _i32, _vp])
 
@@ -252,6 +259,71 @@ def paged_attention_prefill(out, q, key_cache, value_cache, block_tables, contex
                                          int(max_query_len), H, hk, D, bs, nb, float(scale),
                                          _dtype_code(key_cache), _stream_ptr(stream, dev))
     _check(rc, "pa_paged_attention_prefill")
+
+
+def prefix_groups(block_tables, context_lens, block_size: int, max_members: int = 8,
+                  min_shared_blocks: int = 1):
+    """Host: groups of sequences whose tables start with the same full blocks.
+
+    Returns (prefix_lens int32 [B], group_members int32 [num_groups, max_members])."""
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B = cl.shape[0]
+    pl = np.zeros(max(B, 1), np.int32)
+    gm = np.full((max(B, 1), max_members), -1, np.int32)
+    ng = ctypes.c_int(0)
+    _check(_lib.pa_prefix_groups(bt.ctypes.data, cl.ctypes.data, B, bt.shape[1] if bt.ndim == 2 else 0,
+                                 block_size, max_members, min_shared_blocks, pl.ctypes.data, gm.ctypes.data,
+                                 ctypes.byref(ng)), "pa_prefix_groups")
+    return pl[:B].copy(), gm[: ng.value].copy()
+
+
+def decode_shared_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                                  partition_size: int = 0) -> int:
+    return int(_lib.pa_decode_shared_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len,
+                                                     partition_size))
+
+
+def paged_attention_decode_shared(out, q, key_cache, value_cache, block_tables, context_lens, prefix_lens,
+                                  group_members, scale: float, max_context_len: int = 0,
+                                  max_prefix_len: int | None = None, partition_size: int = 0, workspace=None,
+                                  stream=None) -> None:
+    """Decode that reads each group's shared prefix once for all its members.
+
+    prefix_lens int32 [B] and group_members int32 [G, M] as from prefix_groups
+    (device tensors). Same result as paged_attention_decode."""
+    torch = _torch()
+    dev = key_cache.device
+    _cuda(key_cache, "key_cache")
+    _cuda(value_cache, "value_cache", key_cache.dtype, dev)
+    _cuda(q, "q", key_cache.dtype, dev)
+    _cuda(out, "out", key_cache.dtype, dev)
+    for t, n in ((block_tables, "block_tables"), (context_lens, "context_lens"), (prefix_lens, "prefix_lens"),
+                 (group_members, "group_members")):
+        _cuda(t, n, torch.int32, dev)
+    nb, bs, hk, d = key_cache.shape
+    B, H, D = q.shape
+    if D != d or tuple(out.shape) != (B, H, D) or block_tables.shape[0] != B or prefix_lens.shape[0] != B:
+        raise ValueError("shape mismatch")
+    if group_members.dim() != 2:
+        raise ValueError("group_members must be [num_groups, max_members]")
+    mb = block_tables.shape[1]
+    mctx = max_context_len or mb * bs
+    mpre = mctx if max_prefix_len is None else int(max_prefix_len)
+    sp = _stream_ptr(stream, dev)
+    need = decode_shared_workspace_bytes(B, H, D, mctx, partition_size)
+    if workspace is None:
+        workspace = _workspace(dev, sp, need)
+    _cuda(workspace, "workspace", torch.uint8, dev)
+    ng, mm = group_members.shape
+    rc = _lib.pa_paged_attention_decode_shared(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
+                                               value_cache.data_ptr(), block_tables.data_ptr(), mb,
+                                               context_lens.data_ptr(), prefix_lens.data_ptr(),
+                                               group_members.data_ptr() if ng else None, ng, max(mm, 1), mpre,
+                                               B, H, hk, D, bs, nb, float(scale), int(max_context_len),
+                                               int(partition_size), workspace.data_ptr(), workspace.numel(),
+                                               _dtype_code(key_cache), sp)
+    _check(rc, "pa_paged_attention_decode_shared")
 
 
 def copy_blocks(key_cache, value_cache, src_dst_pairs, stream=None) -> None:

@@ -12,7 +12,9 @@
 // Unlike the teaching listing, every failure is reported: an empty free stack
 // (including during copy-on-write), an unknown sequence id, a double add.
 // append() is all-or-nothing.
+#include <algorithm>
 #include <cstdint>
+#include <map>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -234,6 +236,56 @@ int pa_alloc_get_stats(const pa_allocator *a, pa_alloc_stats *out) {
     out->peak_used = a->peak_used;
     out->num_cow_copies = a->cow_copies;
     out->num_seqs = (int64_t)a->seqs.size();
+    return PA_OK;
+}
+
+int pa_prefix_groups(const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                     int max_blocks_per_seq, int block_size, int max_members, int min_shared_blocks,
+                     int32_t *prefix_lens, int32_t *group_members, int *num_groups) {
+    if (num_seqs < 0 || max_blocks_per_seq < 0 || block_size <= 0 || max_members < 2 || min_shared_blocks < 1 ||
+        !num_groups || (num_seqs > 0 && (!block_tables || !context_lens || !prefix_lens || !group_members)))
+        return PA_ERR_INVALID_ARG;
+    *num_groups = 0;
+    try {
+        // candidates keyed by their first physical block, in sequence order
+        std::map<int32_t, std::vector<int>> by_first;
+        for (int b = 0; b < num_seqs; ++b) {
+            prefix_lens[b] = 0;
+            const int full = std::min(context_lens[b] / block_size, max_blocks_per_seq);
+            if (full >= min_shared_blocks && block_tables[(int64_t)b * max_blocks_per_seq] >= 0)
+                by_first[block_tables[(int64_t)b * max_blocks_per_seq]].push_back(b);
+        }
+        int ng = 0;
+        for (auto &kv : by_first) {
+            const std::vector<int> &mem = kv.second;
+            if (mem.size() < 2) continue;
+            for (size_t c0 = 0; c0 < mem.size(); c0 += (size_t)max_members) {
+                const size_t c1 = std::min(mem.size(), c0 + (size_t)max_members);
+                if (c1 - c0 < 2) continue;
+                // leading blocks identical in every member and full in every member's context
+                int shared = max_blocks_per_seq;
+                for (size_t i = c0; i < c1; ++i)
+                    shared = std::min(shared, context_lens[mem[i]] / block_size);
+                const int32_t *lead = block_tables + (int64_t)mem[c0] * max_blocks_per_seq;
+                int j = 0;
+                for (; j < shared; ++j) {
+                    bool same = lead[j] >= 0;
+                    for (size_t i = c0 + 1; i < c1 && same; ++i)
+                        same = block_tables[(int64_t)mem[i] * max_blocks_per_seq + j] == lead[j];
+                    if (!same) break;
+                }
+                if (j < min_shared_blocks) continue;
+                int32_t *row = group_members + (int64_t)ng * max_members;
+                for (int i = 0; i < max_members; ++i)
+                    row[i] = (size_t)i < c1 - c0 ? (int32_t)mem[c0 + (size_t)i] : -1;
+                for (size_t i = c0; i < c1; ++i) prefix_lens[mem[i]] = j * block_size;
+                ++ng;
+            }
+        }
+        *num_groups = ng;
+    } catch (...) {
+        return PA_ERR_OUT_OF_BLOCKS;
+    }
     return PA_OK;
 }
 

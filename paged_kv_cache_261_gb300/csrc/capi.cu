@@ -209,6 +209,127 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
     return rc == 0 ? PA_OK : PA_ERR_CUDA;
 }
 
+size_t pa_decode_shared_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                        int partition_size) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size < 0) return 0;
+    const int part = resolve_partition(partition_size);
+    const int64_t P = num_partitions(max_context_len, part) + 1;
+    return align256((size_t)(num_seqs * (int64_t)num_heads * P * 2 * 4)) +
+           (size_t)(num_seqs * (int64_t)num_heads * P * head_dim * 4);
+}
+
+int pa_paged_attention_decode_shared(void *out, const void *q, const void *key_cache, const void *value_cache,
+                                     const int32_t *block_tables, int max_blocks_per_seq,
+                                     const int32_t *context_lens, const int32_t *prefix_lens,
+                                     const int32_t *group_members, int num_groups, int max_members,
+                                     int max_prefix_len, int num_seqs, int num_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int64_t num_blocks, float scale,
+                                     int max_context_len, int partition_size, void *workspace,
+                                     size_t workspace_bytes, int dtype, void *stream) {
+    if (elem_size(dtype) == 0 || num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+        max_blocks_per_seq <= 0 || max_context_len < 0 || partition_size < 0 || num_groups < 0 ||
+        max_prefix_len < 0 || (num_groups > 0 && max_members < 1))
+        return PA_ERR_INVALID_ARG;
+    if (partition_size != 0 && partition_size % 128 != 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens || !prefix_lens ||
+        (num_groups > 0 && !group_members))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    if (!(scale > 0.f)) return PA_ERR_INVALID_ARG;
+    const int64_t table_cap = (int64_t)max_blocks_per_seq * block_size;
+    const int64_t max_ctx = max_context_len == 0 ? table_cap : max_context_len;
+    if (max_ctx > INT32_MAX || num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    const int part = resolve_partition(partition_size);
+    const int64_t P = num_partitions(max_ctx, part) + 1;
+    if (P > INT32_MAX / part) return PA_ERR_UNSUPPORTED;
+    int64_t limit = (P - 1) * part < table_cap ? (P - 1) * part : table_cap;
+    if (limit > max_ctx) limit = max_ctx;
+
+    pa::DecodeParams d{};
+    d.out = out;
+    d.q = q;
+    d.key_cache = key_cache;
+    d.value_cache = value_cache;
+    d.block_tables = block_tables;
+    d.context_lens = context_lens;
+    d.prefix_lens = prefix_lens;
+    d.num_blocks = num_blocks;
+    d.max_blocks_per_seq = max_blocks_per_seq;
+    d.num_seqs = num_seqs;
+    d.num_heads = num_heads;
+    d.num_kv_heads = num_kv_heads;
+    d.group = num_heads / num_kv_heads;
+    d.head_dim = head_dim;
+    d.block_size = block_size;
+    d.log2_block_size = ilog2(block_size);
+    d.partition_size = part;
+    d.max_partitions = (int)P;
+    d.context_limit = (int)limit;
+    d.scale_log2 = scale * pa::kLog2e;
+    if (!pa::decode_tc_supported(d, dtype)) return PA_ERR_UNSUPPORTED;
+    if (int rc = error_word(&d.err)) return rc;
+
+    pa::PrefillParams g{};
+    g.out = out;
+    g.q = q;
+    g.key_cache = key_cache;
+    g.value_cache = value_cache;
+    g.block_tables = block_tables;
+    g.context_lens = context_lens;
+    g.err = d.err;
+    g.num_blocks = num_blocks;
+    g.num_query_tokens = num_seqs;
+    g.max_blocks_per_seq = max_blocks_per_seq;
+    g.num_seqs = num_seqs;
+    g.num_heads = num_heads;
+    g.num_kv_heads = num_kv_heads;
+    g.group = d.group;
+    int gp = 1;
+    while (gp < g.group) gp <<= 1;
+    g.group_pad = gp;
+    g.rows_q = 128 / gp;
+    g.head_dim = head_dim;
+    g.block_size = block_size;
+    g.log2_block_size = d.log2_block_size;
+    g.context_limit = (int)limit;
+    g.scale_log2 = d.scale_log2;
+    g.prefix_lens = prefix_lens;
+    g.group_members = group_members;
+    g.num_groups = num_groups;
+    g.max_members = max_members;
+    g.partition_size = part;
+    g.max_partitions = (int)P;
+    g.shared_parts = (int)num_partitions(max_prefix_len < limit ? max_prefix_len : limit, part);
+    if (max_prefix_len == 0) g.shared_parts = 0;
+    if (num_groups > 0 && (max_members > g.rows_q || !pa::prefill_tc_supported(g, dtype))) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)num_groups * num_kv_heads * (g.shared_parts + 1) > INT32_MAX) return PA_ERR_UNSUPPORTED;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t need = pa_decode_shared_workspace_bytes(num_seqs, num_heads, head_dim, (int)max_ctx, part);
+    void *ws = workspace;
+    bool owned = false;
+    if (ws) {
+        if (workspace_bytes < need) return PA_ERR_WORKSPACE;
+        if (!aligned16(ws)) return PA_ERR_INVALID_ARG;
+    } else {
+        if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return PA_ERR_CUDA;
+        owned = true;
+    }
+    d.ws_ml = g.ws_ml = static_cast<float *>(ws);
+    d.ws_o = g.ws_o = reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                                align256((size_t)num_seqs * num_heads * P * 2 * 4));
+    int rc = 0;
+    if (num_groups > 0 && g.shared_parts > 0) rc = pa::launch_shared_prefix_tc(g, dtype, s);
+    if (rc == 0) rc = pa::launch_decode_tc(d, dtype, s);
+    if (rc == 0) rc = pa::launch_decode_reduce(d, dtype, s);
+    if (owned) cudaFreeAsync(ws, s);
+    if (rc == -2) return PA_ERR_UNSUPPORTED;
+    return rc == 0 ? PA_OK : PA_ERR_CUDA;
+}
+
 int pa_paged_attention_prefill(void *out, const void *q, const void *key_cache, const void *value_cache,
                                const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
                                const int32_t *query_start_loc, int num_seqs, int64_t num_query_tokens,

@@ -395,10 +395,9 @@ __global__ __launch_bounds__(kReduceThreads) void decode_reduce_warp_kernel(cons
     const int64_t row = (int64_t)blockIdx.x * kReduceWarps + (threadIdx.x >> 5);
     if (row >= (int64_t)p.num_seqs * p.num_heads) return;
     const int b = (int)(row / p.num_heads), h = (int)(row % p.num_heads);
-    int ctx = p.context_lens[b];
-    if (ctx < 0 || ctx > p.context_limit) ctx = ctx < 0 ? 0 : p.context_limit;
-    const int nparts = ctx == 0 ? 1 : (ctx + p.partition_size - 1) / p.partition_size;
-    if (nparts <= 1) return;
+    const SeqSplit sp = seq_split(p, b);
+    if (sp.direct) return;                      // the partition kernel wrote the row
+    const int nparts = sp.shared + sp.priv;
     if (p.head_dim == 128) merge_row_warp<T, 4>(p, b, h, nparts);
     else merge_row_warp<T, 2>(p, b, h, nparts);
 }
@@ -410,10 +409,9 @@ __global__ __launch_bounds__(kReduceThreads) void decode_reduce_kernel(const Dec
     __shared__ __align__(16) float part_sum[kReduceWarps * 128];
     __shared__ float ml_s[2];
     const int h = blockIdx.x, b = blockIdx.y;
-    int ctx = p.context_lens[b];
-    if (ctx < 0 || ctx > p.context_limit) ctx = ctx < 0 ? 0 : p.context_limit;
-    const int nparts = ctx == 0 ? 1 : (ctx + p.partition_size - 1) / p.partition_size;
-    if (nparts <= 1) return;
+    const SeqSplit sp = seq_split(p, b);
+    if (sp.direct) return;                      // the partition kernel wrote the row
+    const int nparts = sp.shared + sp.priv;
     if (p.head_dim == 128) merge_row<T, 4>(p, b, h, nparts, part_sum, ml_s);
     else merge_row<T, 2>(p, b, h, nparts, part_sum, ml_s);
 }

@@ -91,7 +91,8 @@ struct Bars {
 };
 
 struct Item {
-    int b, kvh, part, nparts, t0, t1, ntiles;
+    int b, kvh, part, slot, t0, t1, ntiles;
+    bool direct;                                 // write the final row, not a partial
 };
 
 // Items are dealt to CTAs round-robin in order of decreasing size: first every
@@ -105,7 +106,6 @@ __device__ __forceinline__ Item get_item(int idx, const int *prefix, const int *
     Item it;
     const int pair = idx / p.num_kv_heads;
     it.kvh = idx - pair * p.num_kv_heads;
-    int ctx;
     if (pair < n4) {
         int lo = 0, hi = p.num_seqs;              // prefix[lo] <= pair < prefix[hi]
         while (hi - lo > 1) {
@@ -114,17 +114,16 @@ __device__ __forceinline__ Item get_item(int idx, const int *prefix, const int *
         }
         it.b = lo;
         it.part = pair - prefix[lo];
-        ctx = p.context_lens[lo];
-        ctx = ctx < 0 ? 0 : (ctx > p.context_limit ? p.context_limit : ctx);
     } else {
         it.b = order[pair - n4];
-        ctx = p.context_lens[it.b];
-        ctx = ctx < 0 ? 0 : (ctx > p.context_limit ? p.context_limit : ctx);
-        it.part = ctx / p.partition_size;        // the sequence's last (ragged) partition
+        it.part = -1;                            // the sequence's last (ragged) partition
     }
-    it.nparts = ctx == 0 ? 1 : (ctx + p.partition_size - 1) / p.partition_size;
-    it.t0 = it.part * p.partition_size;
-    it.t1 = min(ctx, it.t0 + p.partition_size);
+    const SeqSplit sp = seq_split(p, it.b);
+    if (it.part < 0) it.part = (sp.ctx - sp.ps) / p.partition_size;
+    it.slot = sp.shared + it.part;
+    it.direct = sp.direct;
+    it.t0 = sp.ps + it.part * p.partition_size;
+    it.t1 = min(sp.ctx, it.t0 + p.partition_size);
     it.ntiles = it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
     return it;
 }
@@ -231,18 +230,17 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     int *counts = reinterpret_cast<int *>(smem + kOffMisc + 8);   // [0] = n4, [1] = list length
     unsigned char *code = sP;
     for (int b = tid; b < B; b += kThreads) {
-        int ctx = p.context_lens[b];
-        if (ctx < 0 || ctx > p.context_limit) {
-            if (blockIdx.x == 0) raise_error(p.err, PA_DEVERR_CONTEXT);
-            ctx = ctx < 0 ? 0 : p.context_limit;
-        }
-        const int nfull = ctx / p.partition_size;
-        const int rt = (ctx - nfull * p.partition_size + kTile - 1) / kTile;   // tiles of the ragged rest
+        const int raw = p.context_lens[b];
+        if ((raw < 0 || raw > p.context_limit) && blockIdx.x == 0) raise_error(p.err, PA_DEVERR_CONTEXT);
+        const SeqSplit sp = seq_split(p, b);
+        const int len = sp.ctx - sp.ps;                                      // this pass's tokens
+        const int nfull = len / p.partition_size;
+        const int rt = (len - nfull * p.partition_size + kTile - 1) / kTile;   // tiles of the ragged rest
         const bool rest_is_full = rt * kTile == p.partition_size;           // as many tiles as a full one
         prefix[b + 1] = nfull + (rest_is_full ? 1 : 0);
         // list bucket: 0 = empty context, 1..3 = tiles of the rest (3 = three or more),
         // 4 = no list entry (no ragged rest, or one with the full tile count)
-        code[b] = (unsigned char)(ctx == 0 ? 0 : ((rt == 0 || rest_is_full) ? 4 : min(rt, 3)));
+        code[b] = (unsigned char)(sp.ctx == 0 ? 0 : ((rt == 0 || rest_is_full) ? 4 : min(rt, 3)));
     }
     __syncthreads();
     if (warp == 0) {
@@ -587,7 +585,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                 ok = false;
                 break;
             }
-            if (I.nparts == 1) {
+            if (I.direct) {
 #pragma unroll
                 for (int g = 0; g < GT; ++g)
                     if (g < G) out[(head0 + g) * kD + row] = Elem<T>::from_f(o_acc[g] / l_tot[g]);
@@ -596,7 +594,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
 #pragma unroll
                 for (int g = 0; g < GT; ++g) {
                     if (g < G) {
-                        const int64_t r = (head0 + g) * P + I.part;
+                        const int64_t r = (head0 + g) * P + I.slot;
                         p.ws_o[r * kD + row] = o_acc[g];
                         if (row == 0) {
                             p.ws_ml[2 * r] = m_run[g];

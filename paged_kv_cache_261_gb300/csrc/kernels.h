@@ -19,6 +19,7 @@ struct DecodeParams {
     float *ws_ml;              // [B][H][P][2] running max (log2 units) and sum
     float *ws_o;               // [B][H][P][D] unnormalised partial outputs
     unsigned int *err;         // device error word
+    const int32_t *prefix_lens;  // optional [B]: leading tokens attended by the shared-prefix pass
     int64_t num_blocks;
     int max_blocks_per_seq;
     int num_seqs;
@@ -60,10 +61,23 @@ struct PrefillParams {
     int max_query_len;
     int context_limit;          // max_blocks_per_seq * block_size
     float scale_log2;
+    // shared-prefix decode (group mode): rows are (member, head) pairs of a group
+    const int32_t *prefix_lens;     // [num_seqs] shared leading tokens per sequence
+    const int32_t *group_members;   // [num_groups, max_members], -1 = empty slot
+    int num_groups;
+    int max_members;
+    int partition_size;
+    int max_partitions;             // workspace stride P
+    int shared_parts;               // partitions of the longest shared prefix
+    float *ws_ml;
+    float *ws_o;
 };
 
 bool prefill_tc_supported(const PrefillParams &p, int dtype);
 int launch_prefill_tc(const PrefillParams &p, int dtype, cudaStream_t stream);
+// Group mode of the same kernel: attention of every group member's query over
+// the group's shared prefix, written as split-K partials (slots 0 .. shared-1).
+int launch_shared_prefix_tc(const PrefillParams &p, int dtype, cudaStream_t stream);
 
 int launch_kv_write(const void *k, const void *v, const int32_t *slot_mapping, int64_t num_tokens,
                     void *key_cache, void *value_cache, int64_t num_slots, int row_bytes,
@@ -80,6 +94,30 @@ int launch_decode_simt(const DecodeParams &p, int dtype, cudaStream_t stream);
 // Tensor-core partition kernel (bf16/f16, head_dim 128, group <= 16, block
 // size 8..128). decode_tc_supported tells whether it covers a call.
 bool decode_tc_supported(const DecodeParams &p, int dtype);
+
+#ifdef __CUDACC__
+// How a sequence's context splits between the shared-prefix pass and the
+// per-sequence pass: tokens [0, ps) are covered by `shared` workspace slots
+// written by the shared pass, tokens [ps, ctx) by `priv` partitions starting at
+// slot `shared`. Without prefix_lens, ps = 0. `direct`: a single partition and
+// nothing shared -- the partition kernel writes the final row itself.
+struct SeqSplit {
+    int ctx, ps, shared, priv;
+    bool direct;
+};
+
+__device__ __forceinline__ SeqSplit seq_split(const DecodeParams &p, int b) {
+    SeqSplit s;
+    int ctx = p.context_lens[b];
+    s.ctx = ctx < 0 ? 0 : (ctx > p.context_limit ? p.context_limit : ctx);
+    int ps = p.prefix_lens ? p.prefix_lens[b] : 0;
+    s.ps = ps < 0 ? 0 : (ps > s.ctx ? s.ctx : ps);
+    s.shared = (s.ps + p.partition_size - 1) / p.partition_size;
+    s.priv = (s.ctx - s.ps + p.partition_size - 1) / p.partition_size;
+    s.direct = s.ctx == 0 || (s.shared == 0 && s.priv <= 1);
+    return s;
+}
+#endif
 int launch_decode_tc(const DecodeParams &p, int dtype, cudaStream_t stream);
 
 // Merge of the partials of sequences with more than one partition.

@@ -71,7 +71,8 @@ constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct PItem {
-    int b, kvh, q_row0, nq, pos_first, kmax, ntiles;
+    int b, kvh, q_row0, nq, pos_first, key0, kmax, ntiles;
+    int group, slot, members;      // group mode: group index, partition slot, member count
 };
 
 // Item idx -> (sequence, kv head, query tile); false when the tile is empty or
@@ -94,8 +95,37 @@ __device__ __forceinline__ bool get_pitem(int idx, const PrefillParams &p, PItem
     it.q_row0 = q_start + qi0;
     it.nq = min(p.rows_q, q_len - qi0);
     it.pos_first = ctx - q_len + qi0;
+    it.key0 = 0;
     it.kmax = it.pos_first + it.nq;              // keys 0 .. kmax-1 are visible to some row
     it.ntiles = (it.kmax + kKT - 1) / kKT;
+    return true;
+}
+
+// Group mode: item idx -> (group, kv head, shared partition); the keys are one
+// partition of the group's shared prefix, read through the first member's table.
+__device__ __forceinline__ bool get_gitem(int idx, const PrefillParams &p, PItem &it) {
+    it.slot = idx % p.shared_parts;
+    const int rest = idx / p.shared_parts;
+    it.kvh = rest % p.num_kv_heads;
+    it.group = rest / p.num_kv_heads;
+    const int32_t *mem = p.group_members + (int64_t)it.group * p.max_members;
+    const int lead = mem[0];
+    if (lead < 0 || lead >= p.num_seqs) return false;
+    int n = 1;                                   // members: leading valid ids
+    while (n < p.max_members && mem[n] >= 0 && mem[n] < p.num_seqs) ++n;
+    it.members = n;
+    int ctx = p.context_lens[lead];
+    ctx = ctx < 0 ? 0 : (ctx > p.context_limit ? p.context_limit : ctx);
+    int ps = p.prefix_lens[lead];
+    ps = ps < 0 ? 0 : (ps > ctx ? ctx : ps);
+    it.key0 = it.slot * p.partition_size;
+    if (it.key0 >= ps) return false;
+    it.b = lead;
+    it.kmax = min(ps, it.key0 + p.partition_size);
+    it.ntiles = (it.kmax - it.key0 + kKT - 1) / kKT;
+    it.pos_first = it.kmax - 1;                  // no causal limit: every row sees the whole partition
+    it.q_row0 = 0;
+    it.nq = n;
     return true;
 }
 
@@ -119,7 +149,7 @@ __device__ __forceinline__ float2 unpack2(uint32_t u) {
     }
 }
 
-template <typename T>
+template <typename T, bool kGroup>
 __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
                                                                  const __grid_constant__ CUtensorMap tm_q,
@@ -139,7 +169,8 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = p.group, Gp = p.group_pad;
-    const int total_items = p.num_seqs * p.num_kv_heads * p.qtiles;
+    const int total_items = kGroup ? p.num_groups * p.num_kv_heads * p.shared_parts
+                                   : p.num_seqs * p.num_kv_heads * p.qtiles;
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -177,15 +208,26 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
         bool ok = true;
         for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
             PItem I;
-            if (!get_pitem(idx, p, I)) continue;
+            if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
             const int32_t *table = p.block_tables + (int64_t)I.b * p.max_blocks_per_seq;
             int w = 1;
             if (lane == 0) {
                 w = mbar_wait(q_empty, (n & 1) ^ 1) ? 1 : 0;
                 if (w) {
                     mbar_arrive_expect_tx(q_full, kQBytes);
-                    tma_load_3d(sQ, &tm_q, q_full, 0, I.kvh * G, I.q_row0);
-                    tma_load_3d(sQ + kChunk, &tm_q, q_full, 64, I.kvh * G, I.q_row0);
+                    if constexpr (kGroup) {
+                        // one box of Gp head rows per member slot; empty slots read zeros
+                        const int32_t *mem = p.group_members + (int64_t)I.group * p.max_members;
+                        for (int m = 0; m < p.rows_q; ++m) {
+                            const int row = m < I.members ? mem[m] * p.num_heads + I.kvh * G
+                                                          : p.num_seqs * p.num_heads;
+                            tma_load_2d(sQ + m * Gp * 128, &tm_q, q_full, 0, row);
+                            tma_load_2d(sQ + kChunk + m * Gp * 128, &tm_q, q_full, 64, row);
+                        }
+                    } else {
+                        tma_load_3d(sQ, &tm_q, q_full, 0, I.kvh * G, I.q_row0);
+                        tma_load_3d(sQ + kChunk, &tm_q, q_full, 64, I.kvh * G, I.q_row0);
+                    }
                 }
             }
             w = __shfl_sync(0xffffffffu, w, 0);
@@ -198,7 +240,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                 const int stage = it & 1;
                 int phys = (int)p.num_blocks;
                 if (lane < nbt) {
-                    const int tok = j * kKT + lane * p.block_size;
+                    const int tok = I.key0 + j * kKT + lane * p.block_size;
                     if (tok < I.kmax) {
                         const int e = table[tok >> p.log2_block_size];
                         if (e >= 0 && e < p.num_blocks) phys = e;
@@ -259,7 +301,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
             };
             for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
                 PItem I;
-                if (!get_pitem(idx, p, I)) continue;
+                if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
                 if (!mbar_wait(q_full, n & 1)) {
                     ok = false;
                     break;
@@ -311,9 +353,10 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
         bool ok = true;
         for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
             PItem I;
-            if (!get_pitem(idx, p, I)) continue;
+            if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
             const bool row_valid = qi < I.nq && g < G;
-            const int pos = row_valid ? I.pos_first + qi : -1;
+            // causal position (prefill), or the last shared key (group mode: no causal limit)
+            const int pos = !row_valid ? -1 : (kGroup ? I.kmax - 1 : I.pos_first + qi);
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < I.ntiles; ++j, ++it) {
                 const int buf = it & 1;
@@ -331,7 +374,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
 
                 // Raw scores; the scale (> 0) is folded into the exponent below. Only tiles
                 // reaching past the item's first position need the causal mask.
-                const int k0 = j * kKT;
+                const int k0 = I.key0 + j * kKT;
                 if (k0 + kKT - 1 > I.pos_first) {
 #pragma unroll
                     for (int c = 0; c < kKT; ++c)
@@ -426,6 +469,25 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                 break;
             }
             tc_fence_after();
+            if constexpr (kGroup) {
+                // split-K partial of this member row: unnormalised O, reference max, sum
+                const int64_t wrow = row_valid ? ((int64_t)p.group_members[(int64_t)I.group * p.max_members + qi] *
+                                                      p.num_heads + I.kvh * G + g) * p.max_partitions + I.slot
+                                               : 0;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t o[64];
+                    tmem_ld64(tmem + lane_off + kColO + c * 64, o);
+                    if (row_valid) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + wrow * kD + c * 64);
+#pragma unroll
+                        for (int u = 0; u < 16; ++u)
+                            dst[u] = make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
+                                                 __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]));
+                    }
+                }
+                if (row_valid) *reinterpret_cast<float2 *>(p.ws_ml + 2 * wrow) = make_float2(m_ref, l);
+            } else {
             const float inv = row_valid ? 1.f / l : 0.f;
             T *orow = out + ((int64_t)(I.q_row0 + qi) * p.num_heads + I.kvh * G + g) * kD;
 #pragma unroll
@@ -443,6 +505,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                         *reinterpret_cast<uint4 *>(orow + c * 64 + u * 8) = pk;
                     }
                 }
+            }
             }
             tc_fence_before();
             __syncwarp();
@@ -464,9 +527,9 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
     }
 }
 
-template <typename T>
+template <typename T, bool kGroup>
 int launch_prefill_t(const PrefillParams &p, CUtensorMapDataType dt, cudaStream_t stream) {
-    auto kern = prefill_tc_kernel<T>;
+    auto kern = prefill_tc_kernel<T, kGroup>;
     static bool attr_set[kMaxDevices] = {};
     static int num_sms[kMaxDevices] = {};
     int dev = 0;
@@ -481,18 +544,30 @@ int launch_prefill_t(const PrefillParams &p, CUtensorMapDataType dt, cudaStream_
     if (!make_kv_cache_map(&mk, p.key_cache, p.num_blocks, p.block_size, p.num_kv_heads, dt) ||
         !make_kv_cache_map(&mv, p.value_cache, p.num_blocks, p.block_size, p.num_kv_heads, dt))
         return -1;
-    // queries as [tokens, heads, dims]; one box = 64 dims x Gp heads x QT tokens (128 rows)
     auto enc = tensor_map_encoder();
     if (!enc) return -1;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.num_heads, (cuuint64_t)p.num_query_tokens};
-    cuuint64_t strides[2] = {kD * 2, (cuuint64_t)p.num_heads * kD * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)p.group_pad, (cuuint32_t)p.rows_q};
-    cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&mq, dt, 3, const_cast<void *>(p.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return -1;
-    const int64_t items = (int64_t)p.num_seqs * p.num_kv_heads * p.qtiles;
+    CUresult rc;
+    if (kGroup) {
+        // decode queries as [sequences * heads, dims]; one box = 64 dims x Gp head rows
+        cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.num_seqs * p.num_heads};
+        cuuint64_t strides[1] = {kD * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)p.group_pad};
+        cuuint32_t estr[2] = {1, 1};
+        rc = enc(&mq, dt, 2, const_cast<void *>(p.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        // queries as [tokens, heads, dims]; one box = 64 dims x Gp heads x QT tokens (128 rows)
+        cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.num_heads, (cuuint64_t)p.num_query_tokens};
+        cuuint64_t strides[2] = {kD * 2, (cuuint64_t)p.num_heads * kD * 2};
+        cuuint32_t box[3] = {64, (cuuint32_t)p.group_pad, (cuuint32_t)p.rows_q};
+        cuuint32_t estr[3] = {1, 1, 1};
+        rc = enc(&mq, dt, 3, const_cast<void *>(p.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (rc != CUDA_SUCCESS) return -1;
+    const int64_t items = kGroup ? (int64_t)p.num_groups * p.num_kv_heads * p.shared_parts
+                                 : (int64_t)p.num_seqs * p.num_kv_heads * p.qtiles;
+    if (items == 0) return 0;
     const int grid = (int)(items < num_sms[dev] ? items : num_sms[dev]);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, mq, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
@@ -508,8 +583,16 @@ bool prefill_tc_supported(const PrefillParams &p, int dtype) {
 
 int launch_prefill_tc(const PrefillParams &p, int dtype, cudaStream_t stream) {
     if (!prefill_tc_supported(p, dtype)) return -2;
-    if (dtype == PA_DTYPE_BF16) return launch_prefill_t<__nv_bfloat16>(p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, stream);
-    return launch_prefill_t<__half>(p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, stream);
+    if (dtype == PA_DTYPE_BF16)
+        return launch_prefill_t<__nv_bfloat16, false>(p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, stream);
+    return launch_prefill_t<__half, false>(p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, stream);
+}
+
+int launch_shared_prefix_tc(const PrefillParams &p, int dtype, cudaStream_t stream) {
+    if (!prefill_tc_supported(p, dtype) || p.max_members < 1 || p.max_members * p.group_pad > kRows) return -2;
+    if (dtype == PA_DTYPE_BF16)
+        return launch_prefill_t<__nv_bfloat16, true>(p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, stream);
+    return launch_prefill_t<__half, true>(p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, stream);
 }
 
 }  // namespace pa

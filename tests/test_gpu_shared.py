@@ -1,0 +1,109 @@
+"""Sharing-aware decode (each group's shared prefix read once) against the oracle
+and against the plain decode, on prefix-sharing layouts produced by forks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_cases import assert_close, dev, oracle_decode, pa_mod, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _free_memory():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+@pytest.fixture(scope="module")
+def pa():
+    return pa_mod()
+
+
+def _shared_prefix_state(num_prompts):
+    """Final tables of the shared-prefix sampling script (the oracle's block manager)."""
+    sc = workloads.shared_prefix(num_prompts=num_prompts)
+    nb = sc.pool_blocks()
+    model = oracle.BlockPoolModel(nb, sc.block_size)
+    for p in range(sc.num_prompts):
+        model.add_seq(p)
+        model.append(p, sc.prompt_len)
+        for j in range(sc.samples_per_prompt):
+            model.fork(p, 1000 + p * sc.samples_per_prompt + j)
+        model.free_seq(p)
+    for s in range(sc.num_samples):
+        model.append(1000 + s, int(sc.private[s]) + 1)
+    ids = np.arange(sc.num_samples) + 1000
+    mb = max(len(model.block_table(int(i))) for i in ids)
+    tables = np.full((sc.num_samples, mb), -1, np.int32)
+    for r, i in enumerate(ids):
+        t = model.block_table(int(i))
+        tables[r, : len(t)] = t
+    return sc, sc.workload(tables, nb)
+
+
+def _run(pa, w, max_members, partition_size=0):
+    d = dev()
+    dt = workloads.torch_dtype(w.dtype)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    kc = torch.full(shape, float("nan"), dtype=dt, device=d)
+    vc = torch.full(shape, float("nan"), dtype=dt, device=d)
+    w.fill_cache_torch(kc, vc, include_newest=True)
+    q = w.q_values(like=kc).to(dt).contiguous()
+    bt = torch.as_tensor(w.block_tables, device=d)
+    cl = torch.as_tensor(w.context_lens, device=d)
+    pl, gm = pa.prefix_groups(w.block_tables, w.context_lens, w.block_size, max_members)
+    plain = torch.full_like(q, float("nan"))
+    pa.paged_attention_decode(plain, q, kc, vc, bt, cl, w.scale, partition_size=partition_size)
+    shared = torch.full_like(q, float("nan"))
+    pa.paged_attention_decode_shared(shared, q, kc, vc, bt, cl, torch.as_tensor(pl, device=d),
+                                     torch.as_tensor(gm, device=d), w.scale, partition_size=partition_size,
+                                     max_prefix_len=int(pl.max()) if pl.size else 0)
+    torch.cuda.synchronize()
+    return plain, shared, pl, gm
+
+
+def test_shared_prefix_sampling_reads_prompts_once(pa):
+    sc, w = _shared_prefix_state(num_prompts=8)
+    plain, shared, pl, gm = _run(pa, w, max_members=8)
+    assert gm.shape[0] == sc.num_prompts and np.all(gm >= 0)      # one group of 8 per prompt
+    assert np.all(pl == 62 * 16)                                   # the 62 full prompt blocks
+    assert pa.get_device_error() == 0
+    a, b = to_f64(plain), to_f64(shared)
+    assert np.all(np.isfinite(b))
+    assert np.abs(a - b).max() <= 2e-2
+    seqs = np.arange(0, w.num_seqs, 3)
+    w.slot_mapping = np.full(w.num_seqs, -1, np.int32)             # contents already complete
+    ref = _oracle_full(w, seqs)
+    assert_close(b[seqs], ref, "bf16", "shared-prefix decode")
+
+
+def _oracle_full(w, seqs):
+    view = w.compact_host_view(seqs, include_newest=True)
+    kc = workloads.to_storage_numpy(view["key_cache"], w.dtype)
+    vc = workloads.to_storage_numpy(view["value_cache"], w.dtype)
+    q = workloads.to_storage_numpy(w.q_values()[np.asarray(seqs)], w.dtype)
+    return oracle.paged_attention(q, kc, vc, view["block_tables"], view["context_lens"], w.scale, w.dtype,
+                                  num_threads=oracle.num_host_threads())
+
+
+@pytest.mark.parametrize("H,Hk,max_members,partition", [(32, 8, 8, 0), (64, 8, 16, 256), (16, 16, 4, 128)])
+def test_random_groups_against_oracle(pa, H, Hk, max_members, partition):
+    groups = [(3, 5, 40), (8, 40, 300), (1, 10, 50), (5, 33, 0), (12, 3, 700), (2, 70, 5)]
+    w = workloads.make_shared_groups(17 + H, groups, 6, H, Hk, 128, 16, "bf16")
+    plain, shared, pl, gm = _run(pa, w, max_members, partition)
+    assert gm.shape[0] >= 5 and pl.max() == 70 * 16
+    assert pa.get_device_error() == 0
+    ref = _oracle_full(w, np.arange(w.num_seqs))
+    assert_close(to_f64(shared), ref, "bf16", f"groups H{H}/{Hk}")
+    assert np.abs(to_f64(plain) - to_f64(shared)).max() <= 2e-2
+
+
+def test_no_groups_equals_plain_decode(pa):
+    w = workloads.llama8b_decode(num_seqs=12)
+    plain, shared, pl, gm = _run(pa, w, 8)
+    assert gm.shape[0] == 0 and np.all(pl == 0)
+    assert np.array_equal(to_f64(plain), to_f64(shared))

@@ -622,3 +622,55 @@ def fill_prior_torch(pw: PrefillWorkload, key_cache, value_cache, chunk_tokens: 
         sl = torch.as_tensor(slots[s:s + chunk_tokens], device=dev)
         kflat[sl] = w.kv_rows(TID_K, si, pi).to(key_cache.dtype)
         vflat[sl] = w.kv_rows(TID_V, si, pi).to(value_cache.dtype)
+
+
+def make_shared_groups(seed: int, groups, singles: int, num_heads: int, num_kv_heads: int,
+                       head_dim: int, block_size: int, dtype: str) -> DecodeWorkload:
+    """Sequences sharing leading blocks by reference, as forks produce them.
+
+    groups: list of (members, shared_blocks, max_private) -- each group's members
+    share `shared_blocks` full blocks of one prompt (same physical blocks, same
+    contents) and then hold 0..max_private private tokens each. `singles` more
+    sequences share nothing. Shapes and contents are seeded."""
+    rng = np.random.default_rng(seed)
+    bs = block_size
+    ctx, pkey, plen = [], [], []
+    layout = []                                   # (group id or -1, shared blocks)
+    for gi, (members, shared, max_priv) in enumerate(groups):
+        for _ in range(members):
+            priv = int(rng.integers(0, max_priv + 1))
+            ctx.append(shared * bs + priv)
+            pkey.append(gi)
+            plen.append(shared * bs)
+            layout.append((gi, shared))
+    for _ in range(singles):
+        ctx.append(int(rng.integers(1, 1500)))
+        pkey.append(0)
+        plen.append(0)
+        layout.append((-1, 0))
+    ctx = np.array(ctx, np.int32)
+    B = ctx.shape[0]
+    nb_total = sum(g[1] for g in groups) + int(((ctx + bs - 1) // bs).sum()) + 8
+    num_blocks = int(1.1 * nb_total) + 8
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    mb = max(int(((ctx + bs - 1) // bs).max()), 1)
+    tables = np.full((B, mb), -1, np.int32)
+    off = 0
+    group_blocks = {}
+    for gi, (_, shared, _) in enumerate(groups):
+        group_blocks[gi] = perm[off:off + shared]
+        off += shared
+    for b in range(B):
+        gi, shared = layout[b]
+        n = int((ctx[b] + bs - 1) // bs)
+        if gi >= 0:
+            tables[b, :shared] = group_blocks[gi]
+        for j in range(shared, n):
+            tables[b, j] = perm[off]
+            off += 1
+    own = np.arange(B, dtype=np.int64) + (1 << 20)
+    return DecodeWorkload(
+        name="shared_groups", seed=seed, num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+        block_size=bs, num_blocks=num_blocks, dtype=dtype, scale=1.0 / math.sqrt(head_dim), q_mult=1.0,
+        context_lens=ctx, block_tables=tables, slot_mapping=_newest_slots(ctx, tables, bs), own_key=own,
+        prefix_key=np.array(pkey, np.int64), prefix_len=np.array(plen, np.int64))
