@@ -107,3 +107,43 @@ def test_no_groups_equals_plain_decode(pa):
     plain, shared, pl, gm = _run(pa, w, 8)
     assert gm.shape[0] == 0 and np.all(pl == 0)
     assert np.array_equal(to_f64(plain), to_f64(shared))
+
+
+def test_decode_over_beam_search_beams(pa):
+    """Final beams of the beam-search script: prompt and common history shared by
+    reference. Cache contents are drawn per physical slot, so the oracle reads the
+    very cache the GPU reads, through the same tables."""
+    import sys
+    sys.path.insert(0, __file__.rsplit("/", 1)[0])
+    from test_beam_search import replay
+    sc = workloads.beam_search_script(k=6, steps=40)
+    model = oracle.BlockPoolModel(512, sc.block_size)
+    beams, _, _, _ = replay(model, sc)
+    H, Hk, D, bs, nb = 32, 8, 128, sc.block_size, 512
+    mb = max(len(model.block_table(b)) for b in beams)
+    tables = np.full((len(beams), mb), -1, np.int32)
+    lens = np.zeros(len(beams), np.int32)
+    for r, b in enumerate(beams):
+        t = model.block_table(b)
+        tables[r, : len(t)] = t
+        lens[r] = model.length(b)
+    slots = np.arange(nb * bs, dtype=np.int64)
+    kc = workloads.content_rows(3, 0, slots, np.zeros_like(slots), Hk * D).reshape(nb, bs, Hk, D)
+    vc = workloads.content_rows(3, 1, slots, np.zeros_like(slots), Hk * D).reshape(nb, bs, Hk, D)
+    q = workloads.content_rows(3, 2, np.arange(len(beams), dtype=np.int64), np.zeros(len(beams), np.int64),
+                               H * D).reshape(len(beams), H, D)
+    d = dev()
+    kt = torch.as_tensor(kc).to(torch.bfloat16).to(d)
+    vt = torch.as_tensor(vc).to(torch.bfloat16).to(d)
+    qt = torch.as_tensor(q).to(torch.bfloat16).to(d)
+    pl, gm = pa.prefix_groups(tables, lens, bs, max_members=8)
+    assert gm.shape[0] >= 1 and pl.max() >= sc.prompt_len // bs * bs
+    out = torch.empty_like(qt)
+    pa.paged_attention_decode_shared(out, qt, kt, vt, torch.as_tensor(tables, device=d),
+                                     torch.as_tensor(lens, device=d), torch.as_tensor(pl, device=d),
+                                     torch.as_tensor(gm, device=d), 1.0 / np.sqrt(D), max_prefix_len=int(pl.max()))
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    ref = oracle.paged_attention(workloads.to_storage_numpy(q, "bf16"), workloads.to_storage_numpy(kc, "bf16"),
+                                 workloads.to_storage_numpy(vc, "bf16"), tables, lens, 1.0 / np.sqrt(D), "bf16")
+    assert_close(to_f64(out), ref, "bf16", "beam-search beams")

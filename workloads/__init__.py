@@ -674,3 +674,44 @@ def make_shared_groups(seed: int, groups, singles: int, num_heads: int, num_kv_h
         block_size=bs, num_blocks=num_blocks, dtype=dtype, scale=1.0 / math.sqrt(head_dim), q_mult=1.0,
         context_lens=ctx, block_tables=tables, slot_mapping=_newest_slots(ctx, tables, bs), own_key=own,
         prefix_key=np.array(pkey, np.int64), prefix_len=np.array(plen, np.int64))
+
+
+# ---------------------------------------------------------------------------
+# beam search (fork / prune / copy-on-write of the last block)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class BeamScript:
+    """Seeded beam-search event script.
+
+    A prompt of prompt_len tokens is prefilled, then `steps` decode steps run
+    with beam width k: at each step every surviving beam proposes candidates
+    and k of them survive; parents[s][i] is the beam (index into the previous
+    step's survivors) that survivor i extends. A parent may have several
+    children (they fork) or none (it is dropped). The choices are drawn from
+    the seed -- no model is involved."""
+    seed: int
+    prompt_len: int
+    steps: int
+    k: int
+    block_size: int
+    parents: list
+
+    @property
+    def final_len(self) -> int:
+        return self.prompt_len + self.steps
+
+
+def beam_search_script(seed: int = 1007, prompt_len: int = 64, steps: int = 32, k: int = 4,
+                       block_size: int = 16) -> BeamScript:
+    """Prompt 64 tokens, 32 steps, block size 16 (the shape of the pages' beam demo)."""
+    rng = np.random.default_rng(seed)
+    parents = []
+    width = 1
+    for _ in range(steps):
+        # survivors concentrate on a few parents, as beams do
+        weights = rng.dirichlet(np.full(width, 0.6))
+        parents.append(sorted(int(x) for x in rng.choice(width, size=k, p=weights)))
+        width = k
+    return BeamScript(seed=seed, prompt_len=prompt_len, steps=steps, k=k, block_size=block_size,
+                      parents=parents)
