@@ -22,8 +22,10 @@
 // Roles (192 threads, one persistent CTA per SM):
 //   warp 0     TMA: the item's query rows (3-D map over [tokens, heads, dims]),
 //              then per key tile the K/V boxes of each physical block through
-//              the block table into a 2-stage ring; blocks past the last visible
-//              key load from an out-of-range coordinate (zeros).
+//              the block table into 2-stage K and V rings with separate
+//              barriers (K freed after its S MMA, V after its P.V MMA; each
+//              tile's V is issued after the next tile's K); blocks past the
+//              last visible key load from an out-of-range coordinate (zeros).
 //   warp 1     one thread issues the MMAs and owns tensor memory.
 //   warps 2-5  softmax (scale, causal mask, exp2, P to shared memory, V rows of
 //              keys past the last visible one zeroed) and the epilogue O / l.
@@ -64,7 +66,7 @@ constexpr int kOffV = kOffK + kStages * kKVBytes;
 constexpr int kOffQ = kOffV + kStages * kKVBytes;
 constexpr int kOffP = kOffQ + kQBytes;
 constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 17;
+constexpr int kNumBars = 19;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
@@ -162,8 +164,11 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
     unsigned char *sQ = smem + kOffQ;
     unsigned char *sP = smem + kOffP;
     uint64_t *bb = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint64_t *full = bb, *empty = bb + 2, *s_full = bb + 4, *s_free = bb + 6, *p_full = bb + 8, *o_done = bb + 10;
-    uint64_t *q_full = bb + 12, *q_empty = bb + 13, *o_free = bb + 14;
+    // K and V stages have separate barriers: a K stage is free again as soon as its
+    // S MMA is done, a V stage only after its P.V MMA.
+    uint64_t *k_full = bb, *k_empty = bb + 2, *v_full = bb + 4, *v_empty = bb + 6;
+    uint64_t *s_full = bb + 8, *s_free = bb + 10, *p_full = bb + 12, *o_done = bb + 14;
+    uint64_t *q_full = bb + 16, *q_empty = bb + 17, *o_free = bb + 18;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -174,8 +179,10 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 4);
             mbar_init(&p_full[i], 4);
@@ -203,12 +210,36 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // Per item: the query rows, then per key tile its K, with each tile's V
+        // issued after the next tile's K (K is needed a step earlier than V).
         const int nbt = kKT / p.block_size;
-        uint32_t it = 0, n = 0;
-        bool ok = true;
+        uint32_t it = 0, n = 0, nv = 0;                 // K tiles, items, V tiles issued
+        bool ok = true, v_pending = false;
+        int v_phys = 0, v_kvh = 0;
+        auto issue_v = [&]() -> bool {                  // V of tile nv (block ids saved with its K)
+            const int stage = nv & 1;
+            int w = 1;
+            if (lane == 0) w = mbar_wait(&v_empty[stage], ((nv >> 1) & 1) ^ 1) ? 1 : 0;
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (!w) return false;
+            if (lane == 0) mbar_arrive_expect_tx(&v_full[stage], kKVBytes);
+            __syncwarp();
+            if (lane < nbt) {
+                unsigned char *dv = sV + stage * kKVBytes + lane * p.block_size * 128;
+                tma_load_4d(dv, &tm_v, &v_full[stage], 0, v_kvh, 0, v_phys);
+                tma_load_4d(dv + kChunk, &tm_v, &v_full[stage], 64, v_kvh, 0, v_phys);
+            }
+            ++nv;
+            v_pending = false;
+            return true;
+        };
         for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
             PItem I;
             if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
+            if (v_pending && !issue_v()) {
+                ok = false;
+                break;
+            }
             const int32_t *table = p.block_tables + (int64_t)I.b * p.max_blocks_per_seq;
             int w = 1;
             if (lane == 0) {
@@ -247,31 +278,36 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                         else raise_error(p.err, PA_DEVERR_BLOCK_ID);
                     }
                 }
-                if (lane == 0) w = mbar_wait(&empty[stage], ((it >> 1) & 1) ^ 1) ? 1 : 0;
+                if (lane == 0) w = mbar_wait(&k_empty[stage], ((it >> 1) & 1) ^ 1) ? 1 : 0;
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (!w || *abort_flag) {
                     ok = false;
                     break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(&full[stage], 2 * kKVBytes);
+                if (lane == 0) mbar_arrive_expect_tx(&k_full[stage], kKVBytes);
                 __syncwarp();
                 if (lane < nbt) {
                     unsigned char *dk = sK + stage * kKVBytes + lane * p.block_size * 128;
-                    unsigned char *dv = sV + stage * kKVBytes + lane * p.block_size * 128;
-                    tma_load_4d(dk, &tm_k, &full[stage], 0, I.kvh, 0, phys);
-                    tma_load_4d(dk + kChunk, &tm_k, &full[stage], 64, I.kvh, 0, phys);
-                    tma_load_4d(dv, &tm_v, &full[stage], 0, I.kvh, 0, phys);
-                    tma_load_4d(dv + kChunk, &tm_v, &full[stage], 64, I.kvh, 0, phys);
+                    tma_load_4d(dk, &tm_k, &k_full[stage], 0, I.kvh, 0, phys);
+                    tma_load_4d(dk + kChunk, &tm_k, &k_full[stage], 64, I.kvh, 0, phys);
                 }
+                if (v_pending && !issue_v()) {
+                    ok = false;
+                    break;
+                }
+                v_pending = true;
+                v_phys = phys;
+                v_kvh = I.kvh;
             }
         }
+        if (ok && v_pending && !issue_v()) ok = false;
         if (!ok) {
             *abort_flag = 1;
             raise_error(p.err, PA_DEVERR_WAIT);
         }
         if (lane == 0) {   // drain copies in flight
-            const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
-            for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j & 1], (j >> 1) & 1);
+            for (uint32_t j = it > 2u ? it - 2 : 0; j < it; ++j) mbar_wait(&k_full[j & 1], (j >> 1) & 1);
+            for (uint32_t j = nv > 2u ? nv - 2 : 0; j < nv; ++j) mbar_wait(&v_full[j & 1], (j >> 1) & 1);
             if (n > 0) mbar_wait(q_full, (n - 1) & 1);
         }
     } else if (warp == 1) {
@@ -287,6 +323,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
             auto issue_pv = [&](uint32_t j, bool first) -> bool {
                 if (first && n > 1 && !mbar_wait(o_free, (n - 2) & 1)) return false;
                 if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1)) return false;
+                if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t vb = sV0 + (j & 1) * kKVBytes, pb = sP0 + (j & 1) * kPBytes;
 #pragma unroll
@@ -296,7 +333,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                     mma_f16(tmem + kColO, a, b, idesc_o, (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(&o_done[j & 1]);
-                mma_commit(&empty[j & 1]);
+                mma_commit(&v_empty[j & 1]);
                 return true;
             };
             for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
@@ -309,7 +346,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                 ++n;
                 for (int j = 0; j < I.ntiles; ++j, ++it) {
                     const int stage = it & 1;
-                    if (*abort_flag || !mbar_wait(&full[stage], (it >> 1) & 1) ||
+                    if (*abort_flag || !mbar_wait(&k_full[stage], (it >> 1) & 1) ||
                         !mbar_wait(&s_free[stage], ((it >> 1) & 1) ^ 1)) {
                         ok = false;
                         break;
@@ -323,6 +360,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                                 idesc_s, kk > 0);
                     }
                     mma_commit(&s_full[stage]);
+                    mma_commit(&k_empty[stage]);
                     if (j == I.ntiles - 1) mma_commit(q_empty);
                     if (j > 0 && !issue_pv(it - 1, j == 1)) {
                         ok = false;
@@ -443,7 +481,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                 l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 // key row r past every row's last visible key: its slot may hold anything
                 const bool zero_v = k0 + r >= I.kmax;
-                if (__any_sync(0xffffffffu, zero_v) && !warp_wait(&full[buf], (it >> 1) & 1)) {
+                if (__any_sync(0xffffffffu, zero_v) && !warp_wait(&v_full[buf], (it >> 1) & 1)) {
                     ok = false;
                     break;
                 }
