@@ -53,25 +53,33 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest():
+# Device-code sources of the kernel each workload's roofline line is about; a
+# recorded DRAM-traffic figure is used only while these files are unchanged.
+_KERNEL_SOURCES = {
+    "decode_tc": ["decode_tc.cu", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
+    "prefill_tc": ["prefill_tc.cu", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
+}
+
+
+def source_digest(kernel: str = "decode_tc"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_261_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in _KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel sources."""
+def recorded_traffic(workload: str, kernel: str = "decode_tc"):
+    """DRAM bytes per launch of the workload's dominant kernel from the committed
+    ncu summary, if it was taken on the current sources of that kernel."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f)
         ent = rec.get(workload)
-        if ent and ent.get("source_digest") == source_digest():
+        if ent and ent.get("source_digest") == source_digest(kernel):
             return float(ent["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -368,7 +376,8 @@ def run_prefill(args, device, rank, world):
             "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
                          "peak_kind": "measured bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks
                          else "fallback", "unit": "TFLOP/s", "frac": achieved / peak,
-                         "algorithmic_flops_per_launch": st.flops, "kernel_ms": kern_ms, "traffic": None},
+                         "algorithmic_flops_per_launch": st.flops, "kernel_ms": kern_ms,
+                         "traffic": recorded_traffic("chunked_prefill", "prefill_tc")},
             "gpu_launches": st.launches_per_step * args.steps, "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)
