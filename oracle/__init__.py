@@ -16,6 +16,10 @@ What it computes and where that is defined (web pages, by title and section):
   - chunked-prefill attention: the same per query position, each seeing the
     positions up to its own (demo 1/demo 2 paged steps; "04 - Paged Attention
     实现进度", B.2 and D.2, cu_seqlens_q / query_start_loc);
+  - 8-bit cache (a reading of this project, not on the pages): OCP FP8 E4M3
+    codes with one float32 scale for K and one for V; scatter = nearest code of
+    x / scale (float32 division), decode attention = the float64 attention over
+    decoded(code) * scale (pinned in ``tests/test_oracle_fp8_pins.py``);
   - block manager: see ``allocator_model.py``.
 
 Every function is pinned by tests in ``tests/test_oracle_pins.py`` against
@@ -37,9 +41,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "pagedattn_oracle.c")
 _LIB = os.path.join(_HERE, "_build", "liboracle.so")
 
-OR_F32, OR_F16, OR_BF16, OR_F64 = 0, 1, 2, 3
-_CODES = {"f32": OR_F32, "f16": OR_F16, "bf16": OR_BF16, "f64": OR_F64}
-_NP_STORAGE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "f64": np.float64}
+OR_F32, OR_F16, OR_BF16, OR_F64, OR_E4M3 = 0, 1, 2, 3, 4
+_CODES = {"f32": OR_F32, "f16": OR_F16, "bf16": OR_BF16, "f64": OR_F64, "e4m3": OR_E4M3}
+_NP_STORAGE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "f64": np.float64,
+               "e4m3": np.uint8}
 
 _lib = None
 
@@ -78,6 +83,17 @@ def _load():
         lib.oracle_paged_prefill.argtypes = [vp, vp, vp, vp, c_int, i32p, c_int, i32p, i32p, c_int, c_int,
                                              c_int, c_int, c_int, i64, ctypes.c_double, c_int]
         lib.oracle_paged_prefill.restype = c_int
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = ctypes.c_double
+        lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+        lib.oracle_kv_write_fp8.argtypes = [vp, vp, c_int, i32p, i64, vp, vp, i64, c_int, i64,
+                                            ctypes.c_float, ctypes.c_float]
+        lib.oracle_kv_write_fp8.restype = i64
+        lib.oracle_paged_attention_fp8.argtypes = [vp, vp, c_int, vp, vp, i32p, c_int, i32p, c_int, c_int,
+                                                   c_int, c_int, c_int, i64, ctypes.c_double, ctypes.c_float,
+                                                   ctypes.c_float, c_int]
+        lib.oracle_paged_attention_fp8.restype = c_int
         _lib = lib
     return _lib
 
@@ -196,6 +212,66 @@ def paged_prefill(q, key_cache, value_cache, block_tables, context_lens, query_s
                                   _ptr(cl), _ptr(qs), B, H, hk, D, bs, nb, float(scale), int(num_threads))
     if rc != 0:
         raise ValueError(f"oracle_paged_prefill: {rc}")
+    return out
+
+
+def e4m3_to_float64(codes) -> np.ndarray:
+    """float64 values of E4M3 codes (NaN for the two NaN codes)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    flat = [lib.oracle_e4m3_to_double(int(x)) for x in c.reshape(-1)]
+    return np.asarray(flat, dtype=np.float64).reshape(c.shape)
+
+
+def e4m3_from_float32(x) -> np.ndarray:
+    """Nearest E4M3 codes (ties to even, saturating at 448) of float32 values."""
+    lib = _load()
+    a = np.asarray(x, dtype=np.float32)
+    flat = [lib.oracle_e4m3_from_float(float(v)) for v in a.reshape(-1)]
+    return np.asarray(flat, dtype=np.uint8).reshape(a.shape)
+
+
+def kv_write_fp8(k, v, slot_mapping, key_cache, value_cache, k_scale: float, v_scale: float,
+                 src_dtype: str) -> int:
+    """In place: uint8 E4M3 caches [NB, bs, Hk, D] get rows k/v [T, Hk, D] quantised
+    as code(x / scale) in float32. Returns the number of invalid slots skipped."""
+    lib = _load()
+    k = _check_storage(k, src_dtype)
+    v = _check_storage(v, src_dtype)
+    for c in (key_cache, value_cache):
+        _check_storage(c, "e4m3")
+        if not c.flags.c_contiguous:
+            raise ValueError("caches must be C-contiguous")
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int32)
+    nb, bs = key_cache.shape[0], key_cache.shape[1]
+    row = int(np.prod(key_cache.shape[2:]))
+    rc = lib.oracle_kv_write_fp8(_ptr(k), _ptr(v), _CODES[src_dtype], _ptr(sm), sm.shape[0], _ptr(key_cache),
+                                 _ptr(value_cache), nb, bs, row, float(k_scale), float(v_scale))
+    if rc < 0:
+        raise ValueError(f"oracle_kv_write_fp8: {rc}")
+    return int(rc)
+
+
+def paged_attention_fp8(q, key_cache, value_cache, block_tables, context_lens, scale: float,
+                        k_scale: float, v_scale: float, q_dtype: str, num_threads: int = 1) -> np.ndarray:
+    """float64 out [B, H, D] of decode attention over uint8 E4M3 caches, element =
+    decoded(code) * k_scale (K) or * v_scale (V)."""
+    lib = _load()
+    q = _check_storage(q, q_dtype)
+    kc = _check_storage(key_cache, "e4m3")
+    vc = _check_storage(value_cache, "e4m3")
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, H, D = q.shape
+    nb, bs, hk, d2 = kc.shape
+    if d2 != D or vc.shape != kc.shape or bt.shape[0] != B or cl.shape[0] != B:
+        raise ValueError("shape mismatch")
+    out = np.zeros((B, H, D), dtype=np.float64)
+    rc = lib.oracle_paged_attention_fp8(_ptr(out), _ptr(q), _CODES[q_dtype], _ptr(kc), _ptr(vc), _ptr(bt),
+                                        bt.shape[1], _ptr(cl), B, H, hk, D, bs, nb, float(scale),
+                                        float(k_scale), float(v_scale), int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_attention_fp8: {rc}")
     return out
 
 

@@ -29,6 +29,15 @@
  *
  * Arithmetic is float64. Cache and query elements are read in their storage
  * type (fp32, fp16, bf16 or fp64) and widened exactly to double.
+ *
+ * 8-bit cache (not on the pages; the design notes state the reading): the
+ * cache may hold OCP FP8 E4M3 codes (OCP 8-bit Floating Point Specification,
+ * "E4M3": sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,
+ * S.1111.111 = NaN, largest finite 448). A cache element stands for
+ * decoded(code) * scale, with one float32 scale for all of K and one for all
+ * of V. Writing divides the token's value by the scale in float32 and rounds
+ * the quotient to the nearest code (ties to even mantissa), magnitudes from
+ * 448 up (infinities included) saturating to 448.
  */
 #include <math.h>
 #include <pthread.h>
@@ -36,7 +45,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_F64 = 3 };
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_F64 = 3, OR_E4M3 = 4 };
 
 enum {
     OR_OK = 0,
@@ -53,8 +62,54 @@ static int elem_bytes(int dtype)
     case OR_F16: return 2;
     case OR_BF16: return 2;
     case OR_F64: return 8;
+    case OR_E4M3: return 1;
     default: return 0;
     }
+}
+
+/* OCP FP8 E4M3 -> double, from the format's definition: exponent field 0 holds
+ * the subnormals (m / 8) * 2^-6; otherwise (1 + m / 8) * 2^(e - 7); the
+ * pattern with all exponent and mantissa bits set is NaN (no infinities). */
+static double e4m3_bits_to_double(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);              /* m * 2^-3 * 2^-6 */
+    else
+        v = ldexp((double)(8 + m), e - 10);    /* (8 + m) * 2^-3 * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+double oracle_e4m3_to_double(uint8_t c) { return e4m3_bits_to_double(c); }
+
+/* Nearest E4M3 code to x. The non-negative finite codes 0x00..0x7E are in
+ * increasing order of magnitude, so |x| belongs to code c when it lies between
+ * the midpoints of c with its two neighbours. Midpoints of codes are exact in
+ * double and so is |x|, so every comparison is exact. On a midpoint the code
+ * with the even mantissa (the even code) wins. |x| >= 448 (and infinity)
+ * saturates to 448; NaN gives 0x7F; the sign bit is x's, also for results that
+ * round to zero. */
+uint8_t oracle_e4m3_from_float(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    int c = 0;
+    while (c < 0x7E) {
+        double mid = 0.5 * (e4m3_bits_to_double((uint8_t)c) + e4m3_bits_to_double((uint8_t)(c + 1)));
+        if (a < mid || (a == mid && (c & 1) == 0))
+            break;
+        ++c;
+    }
+    return (uint8_t)(sign | c);
 }
 
 /* IEEE-754 binary16 -> double, from the format's definition. */
@@ -88,6 +143,7 @@ static double load_elem(const void *base, int64_t i, int dtype)
     case OR_F32: return (double)((const float *)base)[i];
     case OR_F16: return half_bits_to_double(((const uint16_t *)base)[i]);
     case OR_BF16: return bf16_bits_to_double(((const uint16_t *)base)[i]);
+    case OR_E4M3: return e4m3_bits_to_double(((const uint8_t *)base)[i]);
     default: return ((const double *)base)[i];
     }
 }
@@ -124,6 +180,48 @@ int64_t oracle_kv_write(const void *k, const void *v, const int32_t *slot_mappin
         int64_t dst = (block * block_size + offset) * row_bytes;
         memcpy((char *)key_cache + dst, (const char *)k + t * row_bytes, (size_t)row_bytes);
         memcpy((char *)value_cache + dst, (const char *)v + t * row_bytes, (size_t)row_bytes);
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------
+ * Scatter into an 8-bit E4M3 cache  [P1 write_kv; P3 B.2 for the slots; the
+ * encoding is this project's reading, see the file header]
+ *
+ * Same slots and layout as oracle_kv_write; each element x of k (v) is stored
+ * as the E4M3 code nearest to the float32 quotient x / k_scale (x / v_scale).
+ * k and v hold fp32, fp16 or bf16 values (all exact in float32).
+ * Returns the number of invalid slots skipped, or OR_ERR_ARG.
+ * ---------------------------------------------------------------------- */
+int64_t oracle_kv_write_fp8(const void *k, const void *v, int src_dtype, const int32_t *slot_mapping,
+                            int64_t num_tokens, uint8_t *key_cache, uint8_t *value_cache,
+                            int64_t num_blocks, int block_size, int64_t row_elems, float k_scale,
+                            float v_scale)
+{
+    if ((src_dtype != OR_F32 && src_dtype != OR_F16 && src_dtype != OR_BF16) || block_size <= 0 ||
+        row_elems <= 0 || num_tokens < 0 || num_blocks < 0 || !(k_scale > 0.0f) || !(v_scale > 0.0f) ||
+        isinf(k_scale) || isinf(v_scale))
+        return OR_ERR_ARG;
+    int64_t bad = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot == -1)
+            continue;
+        if (slot < 0 || slot >= num_blocks * (int64_t)block_size) {
+            bad++;
+            continue;
+        }
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
+        int64_t dst = (block * block_size + offset) * row_elems;
+        for (int64_t i = 0; i < row_elems; ++i) {
+            float xk = (float)load_elem(k, t * row_elems + i, src_dtype);
+            float xv = (float)load_elem(v, t * row_elems + i, src_dtype);
+            float qk = xk / k_scale;           /* float32 division, rounded to nearest */
+            float qv = xv / v_scale;
+            key_cache[dst + i] = oracle_e4m3_from_float(qk);
+            value_cache[dst + i] = oracle_e4m3_from_float(qv);
+        }
     }
     return bad;
 }
@@ -181,6 +279,7 @@ typedef struct {
     int num_seqs, num_heads, num_kv_heads, head_dim, block_size;
     int64_t num_blocks;
     double scale;
+    double k_scale, v_scale;  /* cache element = stored value * scale (1 unless E4M3) */
     int64_t next_item;        /* work counter over (b, kv head) */
     int status;
 } attn_job;
@@ -199,8 +298,8 @@ static int attend_one(attn_job *J, int b, int kvh, double *Kc, double *Vc, doubl
             return OR_ERR_BLOCK_ID;
         int64_t base = ((int64_t)phys * bs + t % bs) * row + (int64_t)kvh * D;
         for (int d = 0; d < D; ++d) {
-            Kc[(int64_t)t * D + d] = load_elem(J->key_cache, base + d, J->cache_dtype);
-            Vc[(int64_t)t * D + d] = load_elem(J->value_cache, base + d, J->cache_dtype);
+            Kc[(int64_t)t * D + d] = load_elem(J->key_cache, base + d, J->cache_dtype) * J->k_scale;
+            Vc[(int64_t)t * D + d] = load_elem(J->value_cache, base + d, J->cache_dtype) * J->v_scale;
         }
     }
     for (int g = 0; g < G; ++g) {
@@ -320,6 +419,30 @@ int oracle_paged_attention(double *out, const void *q, int q_dtype,
     J.num_kv_heads = num_kv_heads; J.head_dim = head_dim; J.block_size = block_size;
     J.num_blocks = num_blocks; J.scale = scale; J.weights = NULL;
     J.weights_b = -1; J.weights_h = -1;
+    J.k_scale = 1.0; J.v_scale = 1.0;
+    return run_attention(&J, num_threads);
+}
+
+/* Decode attention over an E4M3 cache: the same four steps, each cache element
+ * read as decoded(code) * k_scale for K and decoded(code) * v_scale for V (the
+ * product is exact in double). */
+int oracle_paged_attention_fp8(double *out, const void *q, int q_dtype, const uint8_t *key_cache,
+                               const uint8_t *value_cache, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                               int num_heads, int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, double scale, float k_scale, float v_scale,
+                               int num_threads)
+{
+    attn_job J;
+    memset(&J, 0, sizeof J);
+    J.out = out; J.q = q; J.q_dtype = q_dtype;
+    J.key_cache = key_cache; J.value_cache = value_cache; J.cache_dtype = OR_E4M3;
+    J.block_tables = block_tables; J.max_blocks_per_seq = max_blocks_per_seq;
+    J.context_lens = context_lens; J.num_seqs = num_seqs; J.num_heads = num_heads;
+    J.num_kv_heads = num_kv_heads; J.head_dim = head_dim; J.block_size = block_size;
+    J.num_blocks = num_blocks; J.scale = scale; J.weights = NULL;
+    J.weights_b = -1; J.weights_h = -1;
+    J.k_scale = (double)k_scale; J.v_scale = (double)v_scale;
     return run_attention(&J, num_threads);
 }
 
@@ -340,6 +463,7 @@ int oracle_attention_weights(double *weights, double *out, const void *q, int q_
     J.context_lens = context_lens; J.num_seqs = num_seqs; J.num_heads = num_heads;
     J.num_kv_heads = num_kv_heads; J.head_dim = head_dim; J.block_size = block_size;
     J.num_blocks = num_blocks; J.scale = scale;
+    J.k_scale = 1.0; J.v_scale = 1.0;
     J.weights = weights; J.weights_b = b; J.weights_h = h;
     return run_attention(&J, 1);
 }
