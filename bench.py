@@ -56,9 +56,22 @@ def hbm_peak():
 # Device-code sources of the kernel each workload's roofline line is about; a
 # recorded DRAM-traffic figure is used only while these files are unchanged.
 _KERNEL_SOURCES = {
-    "decode_tc": ["decode_tc.cu", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
+    "decode_tc": ["decode_tc.cu", "decode_order.cuh", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
+    "decode_fp8": ["decode_fp8.cu", "decode_order.cuh", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h",
+                   "kernels_fp8.h"],
     "prefill_tc": ["prefill_tc.cu", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
 }
+
+DECODE_WORKLOADS = ("llama8b_decode", "long_context", "mixed_serving")
+FP8_WORKLOADS = tuple(n + "_fp8" for n in DECODE_WORKLOADS)
+
+
+def base_workload(name: str):
+    """(decode workload builder, 8-bit cache?) of a workload name."""
+    fp8 = name.endswith("_fp8")
+    base = name[: -len("_fp8")] if fp8 else name
+    return {"llama8b_decode": workloads.llama8b_decode, "long_context": workloads.long_context,
+            "mixed_serving": workloads.mixed_serving}[base], fp8
 
 
 def source_digest(kernel: str = "decode_tc"):
@@ -162,20 +175,23 @@ class Step:
         self.device = device
         self.copy_pairs = None
         self.copy_bytes = 0
+        self.fp8 = False
         if name == "shared_prefix":
             w, extra = self._shared_prefix_state()
         else:
-            w = {"llama8b_decode": workloads.llama8b_decode, "long_context": workloads.long_context,
-                 "mixed_serving": workloads.mixed_serving}[name]()
+            build_w, self.fp8 = base_workload(name)
+            w = build_w()
             extra = None
         self.w = w
+        self.k_scale = self.v_scale = workloads.FP8_SCALE
         dt = workloads.torch_dtype(w.dtype)
         self.tdtype = dt
         shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
-        self.kc = torch.zeros(shape, dtype=dt, device=device)
-        self.vc = torch.zeros(shape, dtype=dt, device=device)
+        cdt = torch.uint8 if self.fp8 else dt           # 8-bit caches hold E4M3 codes
+        self.kc = torch.zeros(shape, dtype=cdt, device=device)
+        self.vc = torch.zeros(shape, dtype=cdt, device=device)
         w.fill_cache_torch(self.kc, self.vc, include_newest=False)
-        if name == "mixed_serving":
+        if name.startswith("mixed_serving"):
             k, v = w.extra_write_rows(like=self.kc)
             self.slots = torch.as_tensor(w.extra_write_slots, device=device)
         else:
@@ -183,11 +199,11 @@ class Step:
             self.slots = torch.as_tensor(w.slot_mapping, device=device)
         self.k_new = k.to(dt).contiguous()
         self.v_new = v.to(dt).contiguous()
-        if name == "mixed_serving":
+        if name.startswith("mixed_serving"):
             # the decode batch's own newest tokens are already in the cache
             kn, vn = w.newest_kv(like=self.kc)
-            pa.paged_kv_write(kn.to(dt).contiguous(), vn.to(dt).contiguous(),
-                              torch.as_tensor(w.slot_mapping, device=device), self.kc, self.vc)
+            self.write(kn.to(dt).contiguous(), vn.to(dt).contiguous(),
+                       torch.as_tensor(w.slot_mapping, device=device))
         if extra is not None:
             self.copy_pairs = torch.as_tensor(extra, device=device)
             es = 2
@@ -214,10 +230,12 @@ class Step:
             uniq_tokens = int((w.context_lens.astype(np.int64) - pl).sum()) + lead_prefix
             self.unique_kv_bytes = uniq_tokens * w.row_elems * 2 * 2
         es = {"f32": 4, "f16": 2, "bf16": 2}[w.dtype]
-        ab = w.algorithmic_bytes()
+        ce = 1 if self.fp8 else es                        # bytes of one cache element
+        ab = w.algorithmic_bytes(cache_elem_bytes=ce)
         self.decode_bytes = ab["decode"]
+        self.kv_bytes = ab["kv"]
         ntok = int(self.slots.shape[0])
-        self.write_bytes = 2 * 2 * ntok * w.row_elems * es + 4 * ntok
+        self.write_bytes = 2 * ntok * w.row_elems * (es + ce) + 4 * ntok
         self.step_bytes = self.decode_bytes + self.write_bytes + self.copy_bytes
         self.launches_per_step = 1 + (1 if self.copy_pairs is not None else 0) + 1 + (
             1 if pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, self.max_ctx, 0) else 0)
@@ -252,22 +270,33 @@ class Step:
         extra = np.array([[src, dst] for (src, _), dst in zip(pairs, spare)], np.int32)
         return w, extra
 
+    def write(self, k, v, slots):
+        if self.fp8:
+            self.pa.paged_kv_write_fp8(k, v, slots, self.kc, self.vc, self.k_scale, self.v_scale)
+        else:
+            self.pa.paged_kv_write(k, v, slots, self.kc, self.vc)
+
+    def decode(self, q, bt, cl, prefix=None):
+        pa = self.pa
+        if self.shared is not None:
+            pl, gm, mp = self.shared if prefix is None else prefix
+            pa.paged_attention_decode_shared(self.out, q, self.kc, self.vc, bt, cl, pl, gm, self.w.scale,
+                                             max_context_len=self.max_ctx, max_prefix_len=mp, workspace=self.ws)
+        elif self.fp8:
+            pa.paged_attention_decode_fp8(self.out, q, self.kc, self.vc, bt, cl, self.w.scale, self.k_scale,
+                                          self.v_scale, max_context_len=self.max_ctx, workspace=self.ws)
+        else:
+            pa.paged_attention_decode(self.out, q, self.kc, self.vc, bt, cl, self.w.scale,
+                                      max_context_len=self.max_ctx, workspace=self.ws)
+
     def run(self, ev=None):
         """One step; ev = (start, end) CUDA events bracketing the decode call."""
-        pa = self.pa
         if self.copy_pairs is not None:
-            pa.copy_blocks(self.kc, self.vc, self.copy_pairs)
-        pa.paged_kv_write(self.k_new, self.v_new, self.slots, self.kc, self.vc)
+            self.pa.copy_blocks(self.kc, self.vc, self.copy_pairs)
+        self.write(self.k_new, self.v_new, self.slots)
         if ev is not None:
             ev[0].record()
-        if self.shared is not None:
-            pl, gm, mp = self.shared
-            pa.paged_attention_decode_shared(self.out, self.q, self.kc, self.vc, self.bt, self.cl, pl, gm,
-                                             self.w.scale, max_context_len=self.max_ctx, max_prefix_len=mp,
-                                             workspace=self.ws)
-        else:
-            pa.paged_attention_decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl, self.w.scale,
-                                      max_context_len=self.max_ctx, workspace=self.ws)
+        self.decode(self.q, self.bt, self.cl)
         if ev is not None:
             ev[1].record()
 
@@ -282,8 +311,9 @@ class Step:
                 "partition_size": 512,
                 "shared_prefix_decode": self.shared is not None,
                 "unique_kv_bytes": self.unique_kv_bytes,
-                "decode_kernel": os.environ.get("PA_DECODE_KERNEL", "auto"),
-                "l2": f"inputs larger than L2: {w.algorithmic_bytes()['kv'] / 1e9:.2f} GB of K/V read per step "
+                "kv_cache": (f"e4m3 codes, k_scale = v_scale = {self.k_scale:.9g}" if self.fp8 else w.dtype),
+                "decode_kernel": "decode_fp8" if self.fp8 else os.environ.get("PA_DECODE_KERNEL", "auto"),
+                "l2": f"inputs larger than L2: {self.kv_bytes / 1e9:.2f} GB of K/V read per step "
                       f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"}
 
 
@@ -387,39 +417,50 @@ def run_prefill(args, device, rank, world):
 # CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w, n_seqs: int):
-    """Host inputs of the oracle for the first n_seqs sequences (storage dtype)."""
+def oracle_sample(w, n_seqs: int, fp8: bool = False):
+    """Host inputs of the oracle for the first n_seqs sequences (storage dtype;
+    E4M3 codes for an 8-bit cache)."""
     seqs = np.arange(n_seqs)
-    view = w.compact_host_view(seqs, include_newest=False)
-    kc = workloads.to_storage_numpy(view["key_cache"], w.dtype)
-    vc = workloads.to_storage_numpy(view["value_cache"], w.dtype)
+    view = w.compact_host_view(seqs, include_newest=False, codes=fp8)
+    if fp8:
+        kc, vc = view["key_cache"], view["value_cache"]
+    else:
+        kc = workloads.to_storage_numpy(view["key_cache"], w.dtype)
+        vc = workloads.to_storage_numpy(view["value_cache"], w.dtype)
     kn, vn = w.newest_kv()
     row = w.row_elems
     kn = workloads.to_storage_numpy(kn[seqs].reshape(-1, row), w.dtype)
     vn = workloads.to_storage_numpy(vn[seqs].reshape(-1, row), w.dtype)
     q = workloads.to_storage_numpy(w.q_values()[seqs], w.dtype)
     return dict(kc=kc, vc=vc, kn=kn, vn=vn, q=q, slots=view["slot_mapping"], bt=view["block_tables"],
-                cl=view["context_lens"])
+                cl=view["context_lens"], fp8=fp8)
 
 
 def oracle_step(w, s, threads):
+    """One oracle pass over the sample: newest-token scatter, then decode."""
     import oracle
     kc, vc = s["kc"].copy(), s["vc"].copy()
+    if s["fp8"]:
+        S = workloads.FP8_SCALE
+        oracle.kv_write_fp8(s["kn"], s["vn"], s["slots"], kc, vc, S, S, w.dtype)
+        return oracle.paged_attention_fp8(s["q"], kc, vc, s["bt"], s["cl"], w.scale, S, S, w.dtype,
+                                          num_threads=threads)
     oracle.kv_write(s["kn"], s["vn"], s["slots"], kc, vc, w.dtype)
     return oracle.paged_attention(s["q"], kc, vc, s["bt"], s["cl"], w.scale, w.dtype, num_threads=threads)
 
 
-def sample_bytes(w, n_seqs):
+def sample_bytes(w, n_seqs, fp8: bool = False):
     es = {"f32": 4, "f16": 2, "bf16": 2}[w.dtype]
+    ce = 1 if fp8 else es
     ctx = w.context_lens[:n_seqs].astype(np.int64)
     nb = (ctx + w.block_size - 1) // w.block_size
-    return (int(ctx.sum()) * w.row_elems * 2 * es + 2 * n_seqs * w.num_heads * w.head_dim * es
-            + 4 * int(nb.sum()) + 4 * n_seqs + 2 * 2 * n_seqs * w.row_elems * es)
+    return (int(ctx.sum()) * w.row_elems * 2 * ce + 2 * n_seqs * w.num_heads * w.head_dim * es
+            + 4 * int(nb.sum()) + 4 * n_seqs + 2 * n_seqs * w.row_elems * (es + ce))
 
 
-def pick_sample(w, threads, budget_s):
+def pick_sample(w, threads, budget_s, fp8: bool = False):
     """Largest prefix of sequences whose oracle pass fits the time budget."""
-    s1 = oracle_sample(w, 1)
+    s1 = oracle_sample(w, 1, fp8)
     t = time.perf_counter()
     oracle_step(w, s1, threads)
     dt = time.perf_counter() - t
@@ -433,35 +474,45 @@ def pick_sample(w, threads, budget_s):
     return max(n, 1)
 
 
-def cpu_baseline(w, budget_s=15.0):
+def cpu_baseline(w, fp8: bool = False, budget_s=15.0, min_time_s=10.0):
+    """The oracle, as it stands, on the host cores: a prefix of the batch sized to
+    the budget, passes repeated until about min_time_s of CPU work."""
     import oracle
     threads = oracle.num_host_threads()
-    n = pick_sample(w, threads, budget_s)
-    s = oracle_sample(w, n)
+    n = pick_sample(w, threads, budget_s, fp8)
+    s = oracle_sample(w, n, fp8)
+    passes = 0
     t = time.perf_counter()
-    oracle_step(w, s, threads)
-    dt = time.perf_counter() - t
-    return {"value": sample_bytes(w, n) / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+    while True:
+        oracle_step(w, s, threads)
+        passes += 1
+        dt = time.perf_counter() - t
+        if dt >= min_time_s or passes >= 1000:
+            break
+    return {"value": passes * sample_bytes(w, n, fp8) / dt / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
             "sample": f"first {n} of {w.num_seqs} sequences ({int(w.context_lens[:n].sum())} context tokens): "
-                      f"newest-token scatter + decode, one pass, {dt:.2f} s"}
+                      f"newest-token scatter + decode, {passes} passes in {dt:.1f} s"}
 
 
 def run_reference(args):
     import oracle
     name = args.workload
-    w = {"llama8b_decode": workloads.llama8b_decode, "long_context": workloads.long_context,
-         "mixed_serving": workloads.mixed_serving}.get(name, workloads.llama8b_decode)()
+    if name not in DECODE_WORKLOADS + FP8_WORKLOADS:
+        name = "llama8b_decode"
+    build_w, fp8 = base_workload(name)
+    w = build_w()
     threads = oracle.num_host_threads()
     budget = 90.0 / max(args.steps + args.warmup, 1)
-    n = pick_sample(w, threads, budget)
-    s = oracle_sample(w, n)
+    n = pick_sample(w, threads, budget, fp8)
+    s = oracle_sample(w, n, fp8)
     for _ in range(args.warmup):
         oracle_step(w, s, threads)
     t = time.perf_counter()
     for _ in range(args.steps):
         oracle_step(w, s, threads)
     dt = (time.perf_counter() - t) / max(args.steps, 1)
-    value = sample_bytes(w, n) / dt / 1e9
+    value = sample_bytes(w, n, fp8) / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -556,13 +607,14 @@ def run_ours(args):
                      "achieved": achieved, "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "unit": "GB/s", "frac": achieved / peak,
                      "algorithmic_bytes_per_launch": st.decode_bytes,
-                     "decode_ms": decode_ms, "traffic": recorded_traffic(args.workload)},
+                     "decode_ms": decode_ms,
+                     "traffic": recorded_traffic(args.workload, "decode_fp8" if st.fp8 else "decode_tc")},
         "e2e": e2e,
         "gpu_launches": st.launches_per_step * args.steps,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, st.fp8)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -586,17 +638,11 @@ def run_e2e(st: Step, args, device):
     def one():
         for k in host:
             dev_in[k].copy_(host[k], non_blocking=True)
-        pa = st.pa
         if st.copy_pairs is not None:
-            pa.copy_blocks(st.kc, st.vc, st.copy_pairs)
-        pa.paged_kv_write(dev_in["k"], dev_in["v"], dev_in["slots"], st.kc, st.vc)
-        if st.shared is not None:
-            pa.paged_attention_decode_shared(st.out, dev_in["q"], st.kc, st.vc, dev_in["bt"], dev_in["cl"],
-                                             dev_in["pl"], dev_in["gm"], st.w.scale, max_context_len=st.max_ctx,
-                                             max_prefix_len=st.shared[2], workspace=st.ws)
-        else:
-            pa.paged_attention_decode(st.out, dev_in["q"], st.kc, st.vc, dev_in["bt"], dev_in["cl"], st.w.scale,
-                                      max_context_len=st.max_ctx, workspace=st.ws)
+            st.pa.copy_blocks(st.kc, st.vc, st.copy_pairs)
+        st.write(dev_in["k"], dev_in["v"], dev_in["slots"])
+        prefix = (dev_in["pl"], dev_in["gm"], st.shared[2]) if st.shared is not None else None
+        st.decode(dev_in["q"], dev_in["bt"], dev_in["cl"], prefix)
         out_h.copy_(st.out, non_blocking=True)
 
     for _ in range(3):
@@ -621,8 +667,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode",
-                    choices=["llama8b_decode", "long_context", "mixed_serving", "shared_prefix",
-                             "chunked_prefill"])
+                    choices=[*DECODE_WORKLOADS, *FP8_WORKLOADS, "shared_prefix", "chunked_prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

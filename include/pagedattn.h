@@ -61,6 +61,8 @@ extern "C" {
 #define PA_DTYPE_F32  0
 #define PA_DTYPE_F16  1
 #define PA_DTYPE_BF16 2
+#define PA_DTYPE_E4M3 3   /* 8-bit cache storage (see the _fp8 calls); also   */
+                          /* accepted by pa_copy_blocks                        */
 
 /* ---- device error bits (pa_get_device_error) ------------------------------ */
 #define PA_DEVERR_SLOT       0x1u  /* slot not -1 and outside [0, NB*bs)          */
@@ -258,6 +260,56 @@ int pa_paged_attention_decode_noalloc(void *out, const void *q, const void *key_
 int pa_copy_blocks(void *key_cache, void *value_cache, const int32_t *src_dst_pairs,
                    int64_t num_pairs, int64_t num_blocks, int block_size, int num_kv_heads,
                    int head_dim, int dtype, void *stream);
+
+/*
+ * ---- 8-bit (OCP FP8 E4M3) KV cache ------------------------------------------
+ * Not on the pages [P1-P3]; an extension that halves the bytes a decode step
+ * reads. Code format: OCP 8-bit Floating Point Specification, E4M3 (sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, no infinities, 0x7F/0xFF = NaN,
+ * largest finite 448). The caches are uint8 arrays with the usual layout
+ * [num_blocks, block_size, num_kv_heads, head_dim]; a K element stands for
+ * decoded(code) * k_scale and a V element for decoded(code) * v_scale, with one
+ * float32 scale for all of K and one for all of V (both finite and > 0).
+ */
+
+/*
+ * Scatter with quantisation. [P1 write_kv; P3 B.2 for the slots, exactly as
+ * pa_paged_kv_write]
+ * Element x of k[t] is stored as the E4M3 code nearest to the float32 quotient
+ * x / k_scale (IEEE division), ties to the even code, magnitudes >= 448 and
+ * infinities saturating to +-448, NaN to a NaN code; v likewise with v_scale.
+ * k, v: [num_tokens, num_kv_heads, head_dim] of src_dtype (PA_DTYPE_F32, _F16
+ * or _BF16). Slot rules and errors as pa_paged_kv_write. Requires
+ * num_kv_heads*head_dim to be a multiple of 16.
+ */
+int pa_paged_kv_write_fp8(const void *k, const void *v, const int32_t *slot_mapping,
+                          int64_t num_tokens, void *key_cache, void *value_cache,
+                          int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
+                          float k_scale, float v_scale, int src_dtype, void *stream);
+
+/*
+ * Decode attention over E4M3 caches. [P2 demo 2, eq. 4, as
+ * pa_paged_attention_decode]
+ *
+ *   out[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . k_scale*K8[b,t,h/G,:])
+ *                * v_scale*V8[b,t,h/G,:]
+ *
+ * q and out have dtype PA_DTYPE_BF16 or PA_DTYPE_F16. Codes are expanded to
+ * that type exactly; accumulation is fp32. Supported: head_dim 128,
+ * num_heads / num_kv_heads <= 16, block_size a power of two in [8, 128];
+ * PA_ERR_UNSUPPORTED otherwise. Partitions, max_context_len, the workspace
+ * (size from pa_decode_workspace_bytes; NULL = cudaMallocAsync on the stream)
+ * and the device error bits are those of pa_paged_attention_decode. The caches
+ * must hold finite codes: a NaN code is read as NaN on the f16 path and as
+ * 480 on the bf16 path (the write never stores a NaN code from a finite input).
+ */
+int pa_paged_attention_decode_fp8(void *out, const void *q, const void *key_cache,
+                                  const void *value_cache, const int32_t *block_tables,
+                                  int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                  int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int64_t num_blocks, float scale, float k_scale, float v_scale,
+                                  int max_context_len, int partition_size, void *workspace,
+                                  size_t workspace_bytes, int dtype, void *stream);
 
 /*
  * Synchronise `stream`, then read and clear the current device's error word.

@@ -16,10 +16,15 @@ Entry points (same names as the C ABI, without the ``pa_`` prefix):
                                 context_lens, prefix_lens, group_members, scale)
   prefix_groups(block_tables, context_lens, block_size)   (host)
   copy_blocks(key_cache, value_cache, src_dst_pairs)
+  paged_kv_write_fp8(k, v, slot_mapping, key_cache, value_cache, k_scale, v_scale)
+  paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables,
+                             context_lens, scale, k_scale, v_scale)
   get_device_error()
   BlockAllocator: the host block manager (free list, reference counts, fork,
   copy-on-write, block-table and slot-mapping export).
-Cache layout: [num_blocks, block_size, num_kv_heads, head_dim].
+Cache layout: [num_blocks, block_size, num_kv_heads, head_dim]. The _fp8 calls
+take 8-bit caches (torch.uint8 or torch.float8_e4m3fn) holding OCP FP8 E4M3
+codes with one float32 scale for K and one for V.
 """
 from __future__ import annotations
 
@@ -48,7 +53,7 @@ PA_ERR_UNKNOWN_SEQ = -6
 PA_ERR_WORKSPACE = -7
 PA_ERR_EXISTS = -8
 
-PA_DTYPE_F32, PA_DTYPE_F16, PA_DTYPE_BF16 = 0, 1, 2
+PA_DTYPE_F32, PA_DTYPE_F16, PA_DTYPE_BF16, PA_DTYPE_E4M3 = 0, 1, 2, 3
 
 PA_DEVERR_SLOT = 0x1
 PA_DEVERR_BLOCK_ID = 0x2
@@ -78,6 +83,9 @@ _decl("pa_decode_shared_workspace_bytes", [_i32, _i32, _i32, _i32, _i32], _sz)
 _decl("pa_paged_attention_decode_shared", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                            _i32, _i32, _i32, _i32, _i64, _f, _i32, _i32, _vp, _sz, _i32, _vp])
 _decl("pa_prefix_groups", [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, ctypes.POINTER(ctypes.c_int)])
+_decl("pa_paged_kv_write_fp8", [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _f, _f, _i32, _vp])
+_decl("pa_paged_attention_decode_fp8", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                        _i64, _f, _f, _f, _i32, _i32, _vp, _sz, _i32, _vp])
 _decl("pa_paged_attention_prefill", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
                                      _i32, _i64, _f, _i32, _vp])
 
@@ -121,6 +129,16 @@ def _dtype_code(t) -> int:
     if t.dtype not in m:
         raise TypeError(f"unsupported dtype {t.dtype}")
     return m[t.dtype]
+
+
+def _is_fp8_cache(t) -> bool:
+    torch = _torch()
+    return t.dtype == torch.uint8 or t.dtype == getattr(torch, "float8_e4m3fn", None)
+
+
+def _storage_code(t) -> int:
+    """Element code of a cache tensor, 8-bit caches included."""
+    return PA_DTYPE_E4M3 if _is_fp8_cache(t) else _dtype_code(t)
 
 
 def _stream_ptr(stream, device) -> int:
@@ -337,9 +355,73 @@ def copy_blocks(key_cache, value_cache, src_dst_pairs, stream=None) -> None:
         raise ValueError("src_dst_pairs must be [P, 2]")
     nb, bs, hk, d = key_cache.shape
     rc = _lib.pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr(), src_dst_pairs.data_ptr(),
-                             src_dst_pairs.shape[0], nb, bs, hk, d, _dtype_code(key_cache),
+                             src_dst_pairs.shape[0], nb, bs, hk, d, _storage_code(key_cache),
                              _stream_ptr(stream, dev))
     _check(rc, "pa_copy_blocks")
+
+
+def _fp8_caches(key_cache, value_cache, dev):
+    _cuda(key_cache, "key_cache")
+    _cuda(value_cache, "value_cache", key_cache.dtype, dev)
+    if not _is_fp8_cache(key_cache):
+        raise TypeError(f"8-bit caches must be torch.uint8 or torch.float8_e4m3fn, got {key_cache.dtype}")
+    if value_cache.shape != key_cache.shape:
+        raise ValueError("value_cache shape differs from key_cache")
+    return key_cache.shape
+
+
+def paged_kv_write_fp8(k, v, slot_mapping, key_cache, value_cache, k_scale: float, v_scale: float,
+                       stream=None) -> None:
+    """Scatter k/v [T, Hk, D] (fp32/fp16/bf16) into 8-bit caches [NB, bs, Hk, D] as the
+    E4M3 codes of k / k_scale and v / v_scale, at slot_mapping[T]."""
+    torch = _torch()
+    dev = key_cache.device
+    nb, bs, hk, d = _fp8_caches(key_cache, value_cache, dev)
+    _cuda(k, "k", None, dev)
+    _cuda(v, "v", k.dtype, dev)
+    _cuda(slot_mapping, "slot_mapping", torch.int32, dev)
+    T = slot_mapping.shape[0]
+    if tuple(k.shape) != (T, hk, d) or tuple(v.shape) != (T, hk, d):
+        raise ValueError(f"k/v must be [{T}, {hk}, {d}]")
+    rc = _lib.pa_paged_kv_write_fp8(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T, key_cache.data_ptr(),
+                                    value_cache.data_ptr(), nb, bs, hk, d, float(k_scale), float(v_scale),
+                                    _dtype_code(k), _stream_ptr(stream, dev))
+    _check(rc, "pa_paged_kv_write_fp8")
+
+
+def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, context_lens, scale: float,
+                               k_scale: float, v_scale: float, max_context_len: int = 0,
+                               partition_size: int = 0, workspace=None, stream=None) -> None:
+    """Decode attention over 8-bit caches: K = code * k_scale, V = code * v_scale.
+
+    q, out [B, H, 128] bf16 or fp16; other arguments as paged_attention_decode."""
+    torch = _torch()
+    dev = key_cache.device
+    nb, bs, hk, d = _fp8_caches(key_cache, value_cache, dev)
+    _cuda(q, "q", None, dev)
+    _cuda(out, "out", q.dtype, dev)
+    _cuda(block_tables, "block_tables", torch.int32, dev)
+    _cuda(context_lens, "context_lens", torch.int32, dev)
+    B, H, D = q.shape
+    if D != d or tuple(out.shape) != (B, H, D):
+        raise ValueError("q/out must be [B, H, head_dim]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_tables must be [B, MB] and context_lens [B]")
+    mb = block_tables.shape[1]
+    sp = _stream_ptr(stream, dev)
+    need = decode_workspace_bytes(B, H, D, max_context_len or mb * bs, partition_size)
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            workspace = _workspace(dev, sp, need)
+        _cuda(workspace, "workspace", torch.uint8, dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    rc = _lib.pa_paged_attention_decode_fp8(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
+                                            value_cache.data_ptr(), block_tables.data_ptr(), mb,
+                                            context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
+                                            float(k_scale), float(v_scale), int(max_context_len),
+                                            int(partition_size), ws_ptr, ws_bytes, _dtype_code(q), sp)
+    _check(rc, "pa_paged_attention_decode_fp8")
 
 
 def get_device_error(stream=None, device=None) -> int:

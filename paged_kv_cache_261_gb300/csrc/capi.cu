@@ -8,6 +8,7 @@
 #include "../../include/pagedattn.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "kernels_fp8.h"
 
 namespace {
 
@@ -73,6 +74,85 @@ size_t workspace_bytes_for(int64_t B, int64_t H, int64_t D, int64_t P) {
     return align256((size_t)(B * H * P * 2 * 4)) + (size_t)(B * H * P * D * 4);
 }
 
+bool finite_positive(float x) { return x > 0.0f && x <= 3.4028234663852886e38f; }
+
+constexpr int kNothingToDo = 1;
+
+// Host-side validation and parameter set-up shared by the decode entry points
+// (no CUDA call; p.err is left for the caller). Returns PA_OK, kNothingToDo (no
+// sequences) or an error status. P receives the number of partitions per
+// sequence the grid covers.
+int decode_setup(pa::DecodeParams &p, int64_t &P, void *out, const void *q, const void *key_cache,
+                 const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                 const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                 int block_size, int64_t num_blocks, float scale, int max_context_len, int partition_size) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || partition_size < 0)
+        return PA_ERR_INVALID_ARG;
+    if (!pow2(block_size) || block_size > 256) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
+    if (partition_size != 0 && partition_size % 128 != 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return kNothingToDo;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+
+    const int64_t table_cap = (int64_t)max_blocks_per_seq * block_size;
+    const int64_t max_ctx = max_context_len == 0 ? table_cap : max_context_len;
+    if (max_ctx > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    const int part = resolve_partition(partition_size);
+    P = num_partitions(max_ctx, part);
+    if (P > INT32_MAX / part) return PA_ERR_UNSUPPORTED;
+    int64_t limit = P * part < table_cap ? P * part : table_cap;
+    if (limit > max_ctx) limit = max_ctx;
+
+    p.out = out;
+    p.q = q;
+    p.key_cache = key_cache;
+    p.value_cache = value_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.num_blocks = num_blocks;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_heads / num_kv_heads;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.log2_block_size = ilog2(block_size);
+    p.partition_size = part;
+    p.max_partitions = (int)P;
+    p.context_limit = (int)limit;
+    p.scale_log2 = scale * pa::kLog2e;
+    return PA_OK;
+}
+
+// Split-K workspace of a decode call: the caller's (checked) or, when none is
+// given and one is needed, a cudaMallocAsync block returned in *owned for the
+// caller to release after the merge.
+int decode_workspace(pa::DecodeParams &p, int64_t P, void *workspace, size_t workspace_bytes, cudaStream_t s,
+                     void **owned) {
+    *owned = nullptr;
+    const size_t need = workspace_bytes_for(p.num_seqs, p.num_heads, p.head_dim, P);
+    if (need == 0) return PA_OK;
+    void *ws = workspace;
+    if (ws) {
+        if (workspace_bytes < need) return PA_ERR_WORKSPACE;
+        if (!aligned16(ws)) return PA_ERR_INVALID_ARG;
+    } else {
+        if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return PA_ERR_CUDA;
+        *owned = ws;
+    }
+    p.ws_ml = static_cast<float *>(ws);
+    p.ws_o = reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                       align256((size_t)p.num_seqs * p.num_heads * P * 2 * 4));
+    return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -133,80 +213,83 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
                               int64_t num_blocks, float scale, int max_context_len,
                               int partition_size, void *workspace, size_t workspace_bytes,
                               int dtype, void *stream) {
-    if (elem_size(dtype) == 0 || num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
-        num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
-        max_blocks_per_seq <= 0 || max_context_len < 0 || partition_size < 0)
-        return PA_ERR_INVALID_ARG;
-    if (!pow2(block_size) || block_size > 256) return PA_ERR_UNSUPPORTED;
-    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-    if (num_heads / num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
-    if (partition_size != 0 && partition_size % 128 != 0) return PA_ERR_INVALID_ARG;
-    if (num_seqs == 0) return PA_OK;
-    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
-    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
-        return PA_ERR_INVALID_ARG;
-    if (!(scale == scale)) return PA_ERR_INVALID_ARG;
-
-    const int64_t table_cap = (int64_t)max_blocks_per_seq * block_size;
-    const int64_t max_ctx = max_context_len == 0 ? table_cap : max_context_len;
-    if (max_ctx > INT32_MAX) return PA_ERR_UNSUPPORTED;
-    const int part = resolve_partition(partition_size);
-    const int64_t P = num_partitions(max_ctx, part);
-    if (P > INT32_MAX / part) return PA_ERR_UNSUPPORTED;
-    int64_t limit = P * part < table_cap ? P * part : table_cap;
-    if (limit > max_ctx) limit = max_ctx;
-
+    if (elem_size(dtype) == 0) return PA_ERR_INVALID_ARG;
     pa::DecodeParams p{};
-    p.out = out;
-    p.q = q;
-    p.key_cache = key_cache;
-    p.value_cache = value_cache;
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    p.num_blocks = num_blocks;
-    p.max_blocks_per_seq = max_blocks_per_seq;
-    p.num_seqs = num_seqs;
-    p.num_heads = num_heads;
-    p.num_kv_heads = num_kv_heads;
-    p.group = num_heads / num_kv_heads;
-    p.head_dim = head_dim;
-    p.block_size = block_size;
-    p.log2_block_size = ilog2(block_size);
-    p.partition_size = part;
-    p.max_partitions = (int)P;
-    p.context_limit = (int)limit;
-    p.scale_log2 = scale * pa::kLog2e;
-    if (int rc = error_word(&p.err)) return rc;
-
+    int64_t P = 0;
+    int rc = decode_setup(p, P, out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                          num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                          max_context_len, partition_size);
+    if (rc == kNothingToDo) return PA_OK;
+    if (rc != PA_OK) return rc;
+    if ((rc = error_word(&p.err)) != PA_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, P);
-    void *ws = workspace;
-    bool owned = false;
-    if (need > 0) {
-        if (ws) {
-            if (workspace_bytes < need) return PA_ERR_WORKSPACE;
-            if (!aligned16(ws)) return PA_ERR_INVALID_ARG;
-        } else {
-            if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return PA_ERR_CUDA;
-            owned = true;
-        }
-        p.ws_ml = static_cast<float *>(ws);
-        p.ws_o = reinterpret_cast<float *>(static_cast<char *>(ws) +
-                                           align256((size_t)num_seqs * num_heads * P * 2 * 4));
-    }
+    void *owned = nullptr;
+    if ((rc = decode_workspace(p, P, workspace, workspace_bytes, s, &owned)) != PA_OK) return rc;
 
     const DecodeKernel choice = decode_kernel_choice();
-    int rc;
+    int krc;
     if (choice == DecodeKernel::Tc || (choice == DecodeKernel::Auto && pa::decode_tc_supported(p, dtype)))
-        rc = pa::launch_decode_tc(p, dtype, s);
+        krc = pa::launch_decode_tc(p, dtype, s);
     else
-        rc = pa::launch_decode_simt(p, dtype, s);
-    if (rc == 0 && P > 1) rc = pa::launch_decode_reduce(p, dtype, s);
-    if (owned) cudaFreeAsync(ws, s);
-    if (rc == -2) return PA_ERR_UNSUPPORTED;
-    return rc == 0 ? PA_OK : PA_ERR_CUDA;
+        krc = pa::launch_decode_simt(p, dtype, s);
+    if (krc == 0 && P > 1) krc = pa::launch_decode_reduce(p, dtype, s);
+    if (owned) cudaFreeAsync(owned, s);
+    if (krc == -2) return PA_ERR_UNSUPPORTED;
+    return krc == 0 ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_paged_kv_write_fp8(const void *k, const void *v, const int32_t *slot_mapping, int64_t num_tokens,
+                          void *key_cache, void *value_cache, int64_t num_blocks, int block_size,
+                          int num_kv_heads, int head_dim, float k_scale, float v_scale, int src_dtype,
+                          void *stream) {
+    if (elem_size(src_dtype) == 0 || num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!finite_positive(k_scale) || !finite_positive(v_scale)) return PA_ERR_INVALID_ARG;
+    const int64_t row_elems = (int64_t)num_kv_heads * head_dim;
+    if (row_elems % 16 != 0 || row_elems > (int64_t)1 << 28) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !key_cache || !value_cache) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    if (num_blocks > INT64_MAX / block_size) return PA_ERR_INVALID_ARG;
+    if ((num_tokens + 7) / 8 > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    unsigned int *err = nullptr;
+    if (int rc = error_word(&err)) return rc;
+    if (pa::launch_kv_write_fp8(k, v, src_dtype, slot_mapping, num_tokens, key_cache, value_cache,
+                                num_blocks * block_size, (int)row_elems, k_scale, v_scale, err,
+                                static_cast<cudaStream_t>(stream)) != 0)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+int pa_paged_attention_decode_fp8(void *out, const void *q, const void *key_cache, const void *value_cache,
+                                  const int32_t *block_tables, int max_blocks_per_seq,
+                                  const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                  int head_dim, int block_size, int64_t num_blocks, float scale, float k_scale,
+                                  float v_scale, int max_context_len, int partition_size, void *workspace,
+                                  size_t workspace_bytes, int dtype, void *stream) {
+    if (dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F16) return elem_size(dtype) ? PA_ERR_UNSUPPORTED
+                                                                                  : PA_ERR_INVALID_ARG;
+    if (!finite_positive(k_scale) || !finite_positive(v_scale)) return PA_ERR_INVALID_ARG;
+    pa::DecodeParams p{};
+    int64_t P = 0;
+    int rc = decode_setup(p, P, out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                          num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                          max_context_len, partition_size);
+    if (rc == kNothingToDo) return PA_OK;
+    if (rc != PA_OK) return rc;
+    if (!pa::decode_fp8_supported(p, dtype)) return PA_ERR_UNSUPPORTED;
+    if ((rc = error_word(&p.err)) != PA_OK) return rc;
+    p.scale_log2 = scale * k_scale * pa::kLog2e;                  // k_scale folded into the score scale
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *owned = nullptr;
+    if ((rc = decode_workspace(p, P, workspace, workspace_bytes, s, &owned)) != PA_OK) return rc;
+    int krc = pa::launch_decode_fp8(p, v_scale, dtype, s);
+    if (krc == 0 && P > 1) krc = pa::launch_decode_reduce(p, dtype, s);
+    if (owned) cudaFreeAsync(owned, s);
+    if (krc == -2) return PA_ERR_UNSUPPORTED;
+    return krc == 0 ? PA_OK : PA_ERR_CUDA;
 }
 
 size_t pa_decode_shared_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
@@ -386,7 +469,7 @@ int pa_paged_attention_prefill(void *out, const void *q, const void *key_cache, 
 int pa_copy_blocks(void *key_cache, void *value_cache, const int32_t *src_dst_pairs, int64_t num_pairs,
                    int64_t num_blocks, int block_size, int num_kv_heads, int head_dim, int dtype,
                    void *stream) {
-    const int es = elem_size(dtype);
+    const int es = dtype == PA_DTYPE_E4M3 ? 1 : elem_size(dtype);
     if (es == 0 || num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0)
         return PA_ERR_INVALID_ARG;

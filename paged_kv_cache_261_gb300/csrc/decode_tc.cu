@@ -15,18 +15,23 @@
 // accumulators in tensor memory. The tensor cores take the G-fold reuse of each
 // K/V element off the FP32 pipes; the kernel stays bound by HBM.
 //
-// CTA = one persistent worker per SM; 224 threads in four roles:
-//   warp 0    TMA producer: per tile, reads the tile's table entries (one lane
-//             per physical block) and loads each block's K and V rows
-//             (box = 64 dims x block_size tokens of one kv head, 128-byte
-//             swizzle) plus the group's queries into a 3-stage ring. Blocks
-//             past the partition end or with a bad id load from an
-//             out-of-range coordinate, which TMA fills with zeros.
+// CTA = one persistent worker per SM; 288 threads:
+//   warp 0    TMA producer of K: per tile, reads the tile's table entries (one
+//             lane per physical block, from the item's entries read once at
+//             item start) and loads each block's K rows (box = 64 dims x
+//             block_size tokens of one kv head, 128-byte swizzle) plus the
+//             group's queries into a 3-stage ring. Blocks past the partition
+//             end or with a bad id load from an out-of-range coordinate, which
+//             TMA fills with zeros.
+//   warp 7    TMA producer of V into the same stages (its own full barrier).
 //   warp 6    L2 prefetch: walks the same tiles up to kPrefetchTiles ahead of
 //             the producer's loads and pulls their blocks into L2.
-//   warp 1    MMA issuer (one thread) and tensor-memory owner: S for tile i
-//             into a double-buffered S accumulator, then O for tile i-1 once
-//             its probabilities are in shared memory.
+//   warp 1    S MMA issuer (one thread) and tensor-memory owner: S for tile i
+//             into a double-buffered S accumulator.
+//   warp 8    P.V MMA issuer (one thread): O for tile i once its probabilities
+//             are in shared memory and its V has landed. Copy issue and MMA
+//             issue each cost a single thread most of a tile's time when one
+//             thread did both operands, so each operand has its own issuer.
 //   warps 2-5 softmax and output (thread = token for S, thread = dim for O):
 //             scale, mask, tile max through shuffles + shared memory, exp2,
 //             P^T to shared memory (bf16/f16, 128-byte swizzled K-major), zero
@@ -34,14 +39,16 @@
 //             o = o * alpha + O_tile in registers.
 // Work items = (sequence, partition, kv head), dealt to CTAs round-robin in
 // order of decreasing size from a bucketed prefix sum that each CTA builds in
-// shared memory at kernel start (see get_item). Every wait is bounded (see sm100.cuh); on a timeout the
-// kernel sets PA_DEVERR_WAIT, drains its copies and returns.
+// shared memory at kernel start (decode_order.cuh). Every wait is bounded (see
+// sm100.cuh); on a timeout the kernel sets PA_DEVERR_WAIT, drains its copies and
+// returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <type_traits>
 
 #include "common.cuh"
+#include "decode_order.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
 #include "tma_maps.cuh"
@@ -59,10 +66,11 @@ constexpr int kChunkBytes = kTile * 128;          // 128 rows x 64 dims x 2 B
 constexpr int kKVBytes = 2 * kChunkBytes;         // one tile of K (or V), both 64-dim halves
 constexpr int kQBytes = 2 * kN * 128;             // 16 rows x 128 dims
 constexpr int kPBytes = 2 * kN * 128;             // P^T: 16 rows x 128 tokens
-constexpr int kTxBytes = 2 * kKVBytes + kQBytes;  // bytes TMA delivers per stage
-constexpr int kThreads = 224;
+constexpr int kThreads = 288;
+constexpr int kVProdWarp = 7;                     // issues the V boxes
+constexpr int kPvWarp = 8;                        // issues the P.V MMAs
 constexpr int kSoftmaxThreads = 128;
-constexpr int kMaxSeqs = 1024;                    // sequences per launch (the host splits larger batches)
+constexpr int kMaxSeqs = 512;                     // sequences per launch (the host splits larger batches)
 constexpr uint32_t kTmemCols = 64;                // S[2] x 16 + O[2] x 16 columns
 constexpr int kPrefetchTiles = 2;                 // L2 prefetch distance, in tiles, ahead of the loads
 
@@ -74,11 +82,24 @@ constexpr int kOffP = kOffQ + kStages * kQBytes;
 constexpr int kOffRed = kOffP + 2 * kPBytes;                  // float [2][4][16]
 constexpr int kOffLRed = kOffRed + 2 * 4 * kN * 4;            // float [4][16]
 constexpr int kOffBar = kOffLRed + 4 * kN * 4;                // uint64 barriers
-constexpr int kNumBars = 4 * kStages + 12;
+// mbarrier slots, in order; kNumBars counts them
+constexpr int kBarFull = 0;                                   // [kStages] K and Q of the stage landed
+constexpr int kBarEmpty = kBarFull + kStages;                 // [kStages]
+constexpr int kBarSFull = kBarEmpty + kStages;                // [2]
+constexpr int kBarSFree = kBarSFull + 2;                      // [2]
+constexpr int kBarPFull = kBarSFree + 2;                      // [2]
+constexpr int kBarOFull = kBarPFull + 2;                      // [2]
+constexpr int kBarOFree = kBarOFull + 2;                      // [2]
+constexpr int kBarRed = kBarOFree + 2;                        // [2]
+constexpr int kBarFin = kBarRed + 2;                          // [1]
+constexpr int kBarFullV = kBarFin + 1;                        // [kStages] V of the stage landed
+constexpr int kNumBars = kBarFullV + kStages;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;              // tmem base, abort flag, 2 item counts
 constexpr int kOffPrefix = kOffMisc + 32;                     // int [kMaxSeqs + 1]
 constexpr int kOffOrder = kOffPrefix + (kMaxSeqs + 1) * 4;    // int [kMaxSeqs]
-constexpr int kSmemUsed = kOffOrder + kMaxSeqs * 4;
+constexpr int kOffCtx = kOffOrder + kMaxSeqs * 4;             // int [kMaxSeqs] clamped context lengths
+constexpr int kOffPs = kOffCtx + kMaxSeqs * 4;                // int [kMaxSeqs] first token of this pass
+constexpr int kSmemUsed = kOffPs + kMaxSeqs * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;                  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -88,45 +109,11 @@ struct Bars {
     uint64_t *p_full, *o_full;     // [2]
     uint64_t *o_free, *red;        // [2]
     uint64_t *fin;                 // [1]
+    uint64_t *full_v;              // [kStages]
 };
 
-struct Item {
-    int b, kvh, part, slot, t0, t1, ntiles;
-    bool direct;                                 // write the final row, not a partial
-};
-
-// Items are dealt to CTAs round-robin in order of decreasing size: first every
-// partition with the full tile count (partition_size / 128 tiles: the full ones,
-// and last partitions just as long in tiles), then the other last partitions by
-// tile count -- three or more, two, one -- then empty contexts. prefix[] counts
-// full-tile-count partitions per sequence; order[] lists the remaining sequences
-// in that bucket order (stable within a bucket). n4 = prefix[num_seqs].
-__device__ __forceinline__ Item get_item(int idx, const int *prefix, const int *order, int n4,
-                                         const DecodeParams &p) {
-    Item it;
-    const int pair = idx / p.num_kv_heads;
-    it.kvh = idx - pair * p.num_kv_heads;
-    if (pair < n4) {
-        int lo = 0, hi = p.num_seqs;              // prefix[lo] <= pair < prefix[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (prefix[mid] <= pair) lo = mid; else hi = mid;
-        }
-        it.b = lo;
-        it.part = pair - prefix[lo];
-    } else {
-        it.b = order[pair - n4];
-        it.part = -1;                            // the sequence's last (ragged) partition
-    }
-    const SeqSplit sp = seq_split(p, it.b);
-    if (it.part < 0) it.part = (sp.ctx - sp.ps) / p.partition_size;
-    it.slot = sp.shared + it.part;
-    it.direct = sp.direct;
-    it.t0 = sp.ps + it.part * p.partition_size;
-    it.t1 = min(sp.ctx, it.t0 + p.partition_size);
-    it.ntiles = it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
-    return it;
-}
+using decode_order::Item;
+using decode_order::get_item;
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -175,15 +162,16 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     int *prefix = reinterpret_cast<int *>(smem + kOffPrefix);
 
     Bars bars;
-    bars.full = bar_base;
-    bars.empty = bar_base + kStages;
-    bars.s_full = bar_base + 2 * kStages;
-    bars.s_free = bars.s_full + 2;
-    bars.p_full = bars.s_free + 2;
-    bars.o_full = bars.p_full + 2;
-    bars.o_free = bars.o_full + 2;
-    bars.red = bars.o_free + 2;
-    bars.fin = bars.red + 2;
+    bars.full = bar_base + kBarFull;
+    bars.empty = bar_base + kBarEmpty;
+    bars.s_full = bar_base + kBarSFull;
+    bars.s_free = bar_base + kBarSFree;
+    bars.p_full = bar_base + kBarPFull;
+    bars.o_full = bar_base + kBarOFull;
+    bars.o_free = bar_base + kBarOFree;
+    bars.red = bar_base + kBarRed;
+    bars.fin = bar_base + kBarFin;
+    bars.full_v = bar_base + kBarFullV;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = p.group;
@@ -191,6 +179,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.full_v[s], 1);
             mbar_init(&bars.empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -221,74 +210,12 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // Item order (see get_item): per sequence, the count of full-tile-count
-    // partitions goes to prefix[b + 1] and the list bucket of its last partition to
-    // a byte code (in the P buffer, unused until the first tile); warp 0 then
-    // builds the exclusive prefix sum and the bucketed list, deterministically.
-    const int B = p.num_seqs;
+    // Item order (see decode_order.cuh); the byte codes use the P buffer, which is
+    // unused until the first tile.
     int *order = reinterpret_cast<int *>(smem + kOffOrder);
     int *counts = reinterpret_cast<int *>(smem + kOffMisc + 8);   // [0] = n4, [1] = list length
-    unsigned char *code = sP;
-    for (int b = tid; b < B; b += kThreads) {
-        const int raw = p.context_lens[b];
-        if ((raw < 0 || raw > p.context_limit) && blockIdx.x == 0) raise_error(p.err, PA_DEVERR_CONTEXT);
-        const SeqSplit sp = seq_split(p, b);
-        const int len = sp.ctx - sp.ps;                                      // this pass's tokens
-        const int nfull = len / p.partition_size;
-        const int rt = (len - nfull * p.partition_size + kTile - 1) / kTile;   // tiles of the ragged rest
-        const bool rest_is_full = rt * kTile == p.partition_size;           // as many tiles as a full one
-        prefix[b + 1] = nfull + (rest_is_full ? 1 : 0);
-        // list bucket: 0 = empty context, 1..3 = tiles of the rest (3 = three or more),
-        // 4 = no list entry (no ragged rest, or one with the full tile count)
-        code[b] = (unsigned char)(sp.ctx == 0 ? 0 : ((rt == 0 || rest_is_full) ? 4 : min(rt, 3)));
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const int per = (B + 31) / 32;
-        const int lo = lane * per, hi = min(B, lo + per);
-        int s4 = 0, c0 = 0, c1 = 0, c2 = 0, c3 = 0;        // this lane's counts per bucket
-        for (int i = lo; i < hi; ++i) {
-            s4 += prefix[i + 1];
-            const int k = code[i];
-            c0 += k == 0;
-            c1 += k == 1;
-            c2 += k == 2;
-            c3 += k == 3;
-        }
-        int i4 = s4, i0 = c0, i1 = c1, i2 = c2, i3 = c3;     // inclusive scans over lanes
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n4v = __shfl_up_sync(0xffffffffu, i4, o), n0 = __shfl_up_sync(0xffffffffu, i0, o);
-            const int n1 = __shfl_up_sync(0xffffffffu, i1, o), n2 = __shfl_up_sync(0xffffffffu, i2, o);
-            const int n3 = __shfl_up_sync(0xffffffffu, i3, o);
-            if (lane >= o) {
-                i4 += n4v;
-                i0 += n0;
-                i1 += n1;
-                i2 += n2;
-                i3 += n3;
-            }
-        }
-        const int t0 = __shfl_sync(0xffffffffu, i0, 31), t1 = __shfl_sync(0xffffffffu, i1, 31);
-        const int t2 = __shfl_sync(0xffffffffu, i2, 31), t3 = __shfl_sync(0xffffffffu, i3, 31);
-        // list order: bucket 3, 2, 1, then 0
-        int p3 = i3 - c3, p2 = t3 + i2 - c2, p1 = t3 + t2 + i1 - c1, p0 = t3 + t2 + t1 + i0 - c0;
-        int run = i4 - s4;
-        for (int i = lo; i < hi; ++i) {
-            run += prefix[i + 1];
-            prefix[i + 1] = run;
-            const int k = code[i];
-            if (k == 3) order[p3++] = i;
-            else if (k == 2) order[p2++] = i;
-            else if (k == 1) order[p1++] = i;
-            else if (k == 0) order[p0++] = i;
-        }
-        if (lane == 0) prefix[0] = 0;
-        if (lane == 31) {
-            counts[0] = i4;
-            counts[1] = t0 + t1 + t2 + t3;
-        }
-    }
+    const decode_order::SeqCache cache{reinterpret_cast<int *>(smem + kOffCtx), reinterpret_cast<int *>(smem + kOffPs)};
+    decode_order::build(p, prefix, order, counts, sP, cache);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -296,27 +223,28 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     const int n4 = counts[0];
     const int total_items = (counts[0] + counts[1]) * p.num_kv_heads;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == kVProdWarp) {
+        // ------------------------------------------------------------ producers
+        const bool is_v = warp == kVProdWarp;
+        uint64_t *fullb = is_v ? bars.full_v : bars.full;
+        const CUtensorMap *tm = is_v ? &tm_v : &tm_k;
+        unsigned char *dst0 = is_v ? sV : sK;
         const int nbt = kTile / p.block_size;       // physical blocks per tile
         uint32_t it = 0;
         bool ok = true;
         for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-            const Item I = get_item(idx, prefix, order, n4, p);
-            const int32_t *table = p.block_tables + (int64_t)I.b * p.max_blocks_per_seq;
+            const Item I = get_item(idx, prefix, order, n4, p, cache);
+            const decode_order::ItemTable tb = decode_order::load_item_table(p, I, lane);
             const int qrow = I.b * p.num_heads + I.kvh * G;
             for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
                 const int stage = it % kStages;
                 const uint32_t ph = (it / kStages) & 1;
-                const int tstart = I.t0 + tile * kTile;
+                bool live;
+                const int e = decode_order::tile_entry(tb, tile, nbt, lane, &live);
                 int phys = (int)p.num_blocks;           // out of range: TMA fills zeros
-                if (lane < nbt) {
-                    const int tok = tstart + lane * p.block_size;
-                    if (tok < I.t1) {
-                        const int e = table[tok >> p.log2_block_size];
-                        if (e >= 0 && e < p.num_blocks) phys = e;
-                        else raise_error(p.err, PA_DEVERR_BLOCK_ID);
-                    }
+                if (live) {
+                    if (e >= 0 && e < p.num_blocks) phys = e;
+                    else if (!is_v) raise_error(p.err, PA_DEVERR_BLOCK_ID);
                 }
                 int w = 1;
                 if (lane == 0) w = mbar_wait(&bars.empty[stage], ph ^ 1) ? 1 : 0;
@@ -325,20 +253,17 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                     ok = false;
                     break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(&bars.full[stage], kTxBytes);
+                if (lane == 0) mbar_arrive_expect_tx(&fullb[stage], is_v ? kKVBytes : kKVBytes + kQBytes);
                 __syncwarp();
                 if (lane < nbt) {
-                    unsigned char *dk = sK + stage * kKVBytes + lane * p.block_size * 128;
-                    unsigned char *dv = sV + stage * kKVBytes + lane * p.block_size * 128;
-                    tma_load_4d(dk, &tm_k, &bars.full[stage], 0, I.kvh, 0, phys);
-                    tma_load_4d(dk + kChunkBytes, &tm_k, &bars.full[stage], 64, I.kvh, 0, phys);
-                    tma_load_4d(dv, &tm_v, &bars.full[stage], 0, I.kvh, 0, phys);
-                    tma_load_4d(dv + kChunkBytes, &tm_v, &bars.full[stage], 64, I.kvh, 0, phys);
+                    unsigned char *d = dst0 + stage * kKVBytes + lane * p.block_size * 128;
+                    tma_load_4d(d, tm, &fullb[stage], 0, I.kvh, 0, phys);
+                    tma_load_4d(d + kChunkBytes, tm, &fullb[stage], 64, I.kvh, 0, phys);
                 }
-                if (lane == 0) {
+                if (lane == 0 && !is_v) {
                     unsigned char *dq = sQ + stage * kQBytes;
-                    tma_load_2d(dq, &tm_q, &bars.full[stage], 0, qrow);
-                    tma_load_2d(dq + kN * 128, &tm_q, &bars.full[stage], 64, qrow);
+                    tma_load_2d(dq, &tm_q, &fullb[stage], 0, qrow);
+                    tma_load_2d(dq + kN * 128, &tm_q, &fullb[stage], 64, qrow);
                     *loads_issued = it + 1;             // tiles whose loads are issued
                 }
             }
@@ -347,10 +272,9 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             *abort_flag = 1;
             raise_error(p.err, PA_DEVERR_WAIT);
         }
-        // drain: every issued stage's copies must have landed before the CTA exits
         if (lane == 0) {
             const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
-            for (uint32_t j = first; j < it; ++j) mbar_wait(&bars.full[j % kStages], (j / kStages) & 1);
+            for (uint32_t j = first; j < it; ++j) mbar_wait(&fullb[j % kStages], (j / kStages) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -361,29 +285,8 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             const uint32_t sK0 = smem_addr(sK), sV0 = smem_addr(sV), sQ0 = smem_addr(sQ), sP0 = smem_addr(sP);
             uint32_t it = 0;
             bool ok = true;
-            bool have_prev = false;
-            uint32_t prev_it = 0;
-            auto issue_pv = [&](uint32_t j) -> bool {
-                const int buf = j & 1, stage = j % kStages;
-                const uint32_t bph = (j >> 1) & 1;
-                if (!mbar_wait(&bars.p_full[buf], bph)) return false;
-                if (!mbar_wait(&bars.o_free[buf], bph ^ 1)) return false;
-                tc_fence_after();
-                const uint32_t vbase = sV0 + stage * kKVBytes;
-                const uint32_t pbase = sP0 + buf * kPBytes;
-                const uint32_t dcol = tmem + 2 * kN + buf * kN;
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    const uint64_t a = smem_desc(vbase + kk * 2048, kChunkBytes, 1024);
-                    const uint64_t b = smem_desc(pbase + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
-                    mma_f16(dcol, a, b, idesc_o, kk > 0);
-                }
-                mma_commit(&bars.o_full[buf]);
-                mma_commit(&bars.empty[stage]);
-                return true;
-            };
             for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-                const Item I = get_item(idx, prefix, order, n4, p);
+                const Item I = get_item(idx, prefix, order, n4, p, cache);
                 for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
                     const int stage = it % kStages, buf = it & 1;
                     if (*abort_flag || !mbar_wait(&bars.full[stage], (it / kStages) & 1) ||
@@ -404,15 +307,49 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                         mma_f16(dcol, a, b, idesc_s, kk > 0);
                     }
                     mma_commit(&bars.s_full[buf]);
-                    if (have_prev && !issue_pv(prev_it)) {
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                raise_error(p.err, PA_DEVERR_WAIT);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        if (lane == 0) {
+            constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+            const uint32_t idesc_o = instr_desc_f16(kD, kN, kBf16, true, false);
+            const uint32_t sV0 = smem_addr(sV), sP0 = smem_addr(sP);
+            uint32_t it = 0;
+            bool ok = true;
+            auto issue_pv = [&](uint32_t j) -> bool {
+                const int buf = j & 1, stage = j % kStages;
+                const uint32_t bph = (j >> 1) & 1;
+                if (!mbar_wait(&bars.p_full[buf], bph)) return false;
+                if (!mbar_wait(&bars.o_free[buf], bph ^ 1)) return false;
+                if (!mbar_wait(&bars.full_v[stage], (j / kStages) & 1)) return false;
+                tc_fence_after();
+                const uint32_t vbase = sV0 + stage * kKVBytes;
+                const uint32_t pbase = sP0 + buf * kPBytes;
+                const uint32_t dcol = tmem + 2 * kN + buf * kN;
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    const uint64_t a = smem_desc(vbase + kk * 2048, kChunkBytes, 1024);
+                    const uint64_t b = smem_desc(pbase + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+                    mma_f16(dcol, a, b, idesc_o, kk > 0);
+                }
+                mma_commit(&bars.o_full[buf]);
+                mma_commit(&bars.empty[stage]);
+                return true;
+            };
+            for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+                const Item I = get_item(idx, prefix, order, n4, p, cache);
+                for (int tile = 0; tile < I.ntiles; ++tile, ++it)
+                    if (*abort_flag || !issue_pv(it)) {
                         ok = false;
                         break;
                     }
-                    have_prev = true;
-                    prev_it = it;
-                }
             }
-            if (ok && have_prev && !issue_pv(prev_it)) ok = false;
             if (!ok) {
                 *abort_flag = 1;
                 raise_error(p.err, PA_DEVERR_WAIT);
@@ -429,14 +366,12 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         uint32_t n = 0;
         bool go = true;
         for (int idx = blockIdx.x; idx < total_items && go; idx += gridDim.x) {
-            const Item I = get_item(idx, prefix, order, n4, p);
-            const int32_t *table = p.block_tables + (int64_t)I.b * p.max_blocks_per_seq;
+            const Item I = get_item(idx, prefix, order, n4, p, cache);
+            const decode_order::ItemTable tb = decode_order::load_item_table(p, I, lane);
             for (int tile = 0; tile < I.ntiles; ++tile, ++n) {
-                int e = -1;
-                if (lane < nbt) {
-                    const int tok = I.t0 + tile * kTile + lane * p.block_size;
-                    if (tok < I.t1) e = table[tok >> p.log2_block_size];
-                }
+                bool live;
+                int e = decode_order::tile_entry(tb, tile, nbt, lane, &live);
+                if (!live) e = -1;
                 if (n >= *loads_issued + kPrefetchTiles) {
                     const unsigned long long t0 = globaltimer_ns();
                     while (n >= *loads_issued + kPrefetchTiles) {
@@ -466,7 +401,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         bool ok = true;
         float m_run[GT], l_part[GT], o_acc[GT], alpha_prev[GT];
         for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-            const Item I = get_item(idx, prefix, order, n4, p);
+            const Item I = get_item(idx, prefix, order, n4, p, cache);
             const int64_t head0 = (int64_t)I.b * p.num_heads + (int64_t)I.kvh * G;
             if (I.ntiles == 0) {
 #pragma unroll
@@ -538,7 +473,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                 }
                 // masked token: its V row may hold anything (NaN included) and P = 0,
                 // so zero the row once the stage's copies have landed
-                if (__any_sync(0xffffffffu, !valid) && !warp_wait(&bars.full[stage], (it / kStages) & 1)) {
+                if (__any_sync(0xffffffffu, !valid) && !warp_wait(&bars.full_v[stage], (it / kStages) & 1)) {
                     ok = false;
                     break;
                 }

@@ -99,8 +99,10 @@ bool decode_tc_supported(const DecodeParams &p, int dtype);
 // How a sequence's context splits between the shared-prefix pass and the
 // per-sequence pass: tokens [0, ps) are covered by `shared` workspace slots
 // written by the shared pass, tokens [ps, ctx) by `priv` partitions starting at
-// slot `shared`. Without prefix_lens, ps = 0. `direct`: a single partition and
-// nothing shared -- the partition kernel writes the final row itself.
+// slot `shared`. Without prefix_lens, ps = 0. ps is the given prefix length
+// rounded down to whole blocks (both passes round alike), so every pass starts
+// on a block boundary. `direct`: a single partition and nothing shared -- the
+// partition kernel writes the final row itself.
 struct SeqSplit {
     int ctx, ps, shared, priv;
     bool direct;
@@ -111,7 +113,7 @@ __device__ __forceinline__ SeqSplit seq_split(const DecodeParams &p, int b) {
     int ctx = p.context_lens[b];
     s.ctx = ctx < 0 ? 0 : (ctx > p.context_limit ? p.context_limit : ctx);
     int ps = p.prefix_lens ? p.prefix_lens[b] : 0;
-    s.ps = ps < 0 ? 0 : (ps > s.ctx ? s.ctx : ps);
+    s.ps = (ps < 0 ? 0 : (ps > s.ctx ? s.ctx : ps)) & ~(p.block_size - 1);
     s.shared = (s.ps + p.partition_size - 1) / p.partition_size;
     s.priv = (s.ctx - s.ps + p.partition_size - 1) / p.partition_size;
     s.direct = s.ctx == 0 || (s.shared == 0 && s.priv <= 1);

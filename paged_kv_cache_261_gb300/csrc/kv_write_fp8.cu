@@ -1,0 +1,109 @@
+// Scatter of new tokens into an 8-bit (OCP FP8 E4M3) paged cache.
+//
+// The slot arithmetic is that of "PagedAttention实现" write_kv and "04 - Paged
+// Attention 实现进度" B.2 (slot = block * block_size + offset; one token's row of
+// all kv heads is contiguous in the [num_blocks, block_size, num_kv_heads,
+// head_dim] cache). The 8-bit encoding is not on the pages: each element x is
+// stored as the E4M3 code nearest to x / scale, the quotient taken in float32
+// with IEEE division and rounded to the code by the hardware conversion
+// (round to nearest even, saturating to +-448). One warp per token; a lane
+// turns 16 source elements into one 16-byte run of codes.
+#include "common.cuh"
+#include "kernels_fp8.h"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 8;       // tokens per CTA
+
+// 16 consecutive source elements (16-byte aligned) as floats.
+template <typename TS>
+__device__ __forceinline__ void load16(const TS *src, float *f) {
+    constexpr int kPer = Vec16<TS>::N;                 // elements per 16-byte vector
+#pragma unroll
+    for (int u = 0; u < 16 / kPer; ++u) {
+        const uint4 w = __ldcs(reinterpret_cast<const uint4 *>(src) + u);
+        Vec16<TS>::unpack(w, f + u * kPer);
+    }
+}
+
+// Codes of x[0..15] / scale, code i in byte i of the result.
+__device__ __forceinline__ uint4 encode16(const float *x, float scale) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint16_t lo, hi;
+        const float a = __fdiv_rn(x[4 * i], scale), b = __fdiv_rn(x[4 * i + 1], scale);
+        const float c = __fdiv_rn(x[4 * i + 2], scale), d = __fdiv_rn(x[4 * i + 3], scale);
+        // the first source operand lands in the upper byte
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+        w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename TS>
+__global__ __launch_bounds__(kWarps * 32) void kv_write_fp8_kernel(
+    const TS *__restrict__ k, const TS *__restrict__ v, const int32_t *__restrict__ slots, int64_t num_tokens,
+    uint4 *__restrict__ kc, uint4 *__restrict__ vc, int64_t num_slots, int row_elems, float k_scale,
+    float v_scale, unsigned int *err) {
+    // a decode launched after this kernel may start its set-up now; it waits for
+    // this grid to finish before reading the cache
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (t >= num_tokens) return;
+    const int64_t slot = slots[t];
+    if (slot == -1) return;
+    if (slot < 0 || slot >= num_slots) {
+        if (lane == 0) raise_error(err, PA_DEVERR_SLOT);
+        return;
+    }
+    const int groups = row_elems / 16;
+    const TS *ks = k + t * row_elems;
+    const TS *vs = v + t * row_elems;
+    uint4 *kd = kc + slot * groups;
+    uint4 *vd = vc + slot * groups;
+    for (int g = lane; g < groups; g += 32) {
+        float xk[16], xv[16];
+        load16(ks + g * 16, xk);
+        load16(vs + g * 16, xv);
+        kd[g] = encode16(xk, k_scale);
+        vd[g] = encode16(xv, v_scale);
+    }
+}
+
+template <typename TS>
+int launch_t(const void *k, const void *v, const int32_t *slots, int64_t num_tokens, void *kc, void *vc,
+             int64_t num_slots, int row_elems, float k_scale, float v_scale, unsigned int *err,
+             cudaStream_t stream) {
+    const int64_t grid = (num_tokens + kWarps - 1) / kWarps;
+    kv_write_fp8_kernel<TS><<<(unsigned)grid, kWarps * 32, 0, stream>>>(
+        static_cast<const TS *>(k), static_cast<const TS *>(v), slots, num_tokens, static_cast<uint4 *>(kc),
+        static_cast<uint4 *>(vc), num_slots, row_elems, k_scale, v_scale, err);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int launch_kv_write_fp8(const void *k, const void *v, int src_dtype, const int32_t *slot_mapping,
+                        int64_t num_tokens, void *key_cache, void *value_cache, int64_t num_slots,
+                        int row_elems, float k_scale, float v_scale, unsigned int *err, cudaStream_t stream) {
+    if (num_tokens == 0) return 0;
+    switch (src_dtype) {
+    case PA_DTYPE_F32:
+        return launch_t<float>(k, v, slot_mapping, num_tokens, key_cache, value_cache, num_slots, row_elems,
+                               k_scale, v_scale, err, stream);
+    case PA_DTYPE_F16:
+        return launch_t<__half>(k, v, slot_mapping, num_tokens, key_cache, value_cache, num_slots, row_elems,
+                                k_scale, v_scale, err, stream);
+    case PA_DTYPE_BF16:
+        return launch_t<__nv_bfloat16>(k, v, slot_mapping, num_tokens, key_cache, value_cache, num_slots,
+                                       row_elems, k_scale, v_scale, err, stream);
+    default:
+        return -2;
+    }
+}
+
+}  // namespace pa

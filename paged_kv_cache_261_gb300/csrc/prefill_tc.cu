@@ -119,7 +119,7 @@ __device__ __forceinline__ bool get_gitem(int idx, const PrefillParams &p, PItem
     int ctx = p.context_lens[lead];
     ctx = ctx < 0 ? 0 : (ctx > p.context_limit ? p.context_limit : ctx);
     int ps = p.prefix_lens[lead];
-    ps = ps < 0 ? 0 : (ps > ctx ? ctx : ps);
+    ps = (ps < 0 ? 0 : (ps > ctx ? ctx : ps)) & ~(p.block_size - 1);   // whole blocks, as seq_split
     it.key0 = it.slot * p.partition_size;
     if (it.key0 >= ps) return false;
     it.b = lead;

@@ -90,3 +90,52 @@ def check_newest_rows(w: workloads.DecodeWorkload, kc: torch.Tensor, vc: torch.T
     kn, vn = w.newest_kv()
     assert np.array_equal(got_k, kn.reshape(-1, row)[live])
     assert np.array_equal(got_v, vn.reshape(-1, row)[live])
+
+
+# ---------------------------------------------------------------------------
+# 8-bit (E4M3) cache
+# ---------------------------------------------------------------------------
+
+FP8_POISON = 0x7F      # the E4M3 NaN pattern in every slot no context uses
+
+
+def gpu_decode_fp8(w: workloads.DecodeWorkload, partition_size=0, max_context_len=0, write_newest=True,
+                   k_scale=workloads.FP8_SCALE, v_scale=workloads.FP8_SCALE, workspace=None):
+    """uint8 caches filled with codes, the newest tokens scattered (quantised) from
+    w.dtype rows with paged_kv_write_fp8, then the 8-bit decode."""
+    pa = pa_mod()
+    d = dev()
+    dt = workloads.torch_dtype(w.dtype)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    kc = torch.full(shape, FP8_POISON, dtype=torch.uint8, device=d)
+    vc = torch.full(shape, FP8_POISON, dtype=torch.uint8, device=d)
+    w.fill_cache_torch(kc, vc, include_newest=not write_newest)
+    if write_newest:
+        kn, vn = w.newest_kv(like=kc)
+        pa.paged_kv_write_fp8(kn.to(dt).contiguous(), vn.to(dt).contiguous(),
+                              torch.as_tensor(w.slot_mapping, device=d), kc, vc, k_scale, v_scale)
+    q = w.q_values(like=kc).to(dt).contiguous()
+    out = torch.full_like(q, float("nan"))
+    pa.paged_attention_decode_fp8(out, q, kc, vc, torch.as_tensor(w.block_tables, device=d),
+                                  torch.as_tensor(w.context_lens, device=d), w.scale, k_scale, v_scale,
+                                  max_context_len=max_context_len, partition_size=partition_size,
+                                  workspace=workspace)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+def oracle_decode_fp8(w: workloads.DecodeWorkload, seqs, write_newest=True, k_scale=workloads.FP8_SCALE,
+                      v_scale=workloads.FP8_SCALE) -> np.ndarray:
+    """float64 [len(seqs), H, D]: oracle 8-bit scatter of the newest tokens + oracle decode."""
+    seqs = np.asarray(seqs, dtype=np.int64)
+    view = w.compact_host_view(seqs, include_newest=not write_newest, codes=True)
+    kc, vc = view["key_cache"], view["value_cache"]
+    if write_newest:
+        kn, vn = w.newest_kv()
+        row = w.num_kv_heads * w.head_dim
+        oracle.kv_write_fp8(workloads.to_storage_numpy(kn[seqs].reshape(-1, row), w.dtype),
+                            workloads.to_storage_numpy(vn[seqs].reshape(-1, row), w.dtype),
+                            view["slot_mapping"], kc, vc, k_scale, v_scale, w.dtype)
+    q = workloads.to_storage_numpy(w.q_values()[seqs], w.dtype)
+    return oracle.paged_attention_fp8(q, kc, vc, view["block_tables"], view["context_lens"], w.scale,
+                                      k_scale, v_scale, w.dtype, num_threads=oracle.num_host_threads())

@@ -28,6 +28,7 @@ def _declared_functions():
 def test_header_declares_the_boundary_calls():
     names = _declared_functions()
     for must in ("pa_paged_kv_write", "pa_paged_attention_decode", "pa_copy_blocks",
+                 "pa_paged_kv_write_fp8", "pa_paged_attention_decode_fp8",
                  "pa_decode_workspace_bytes", "pa_get_device_error", "pa_alloc_create",
                  "pa_alloc_append", "pa_alloc_fork", "pa_alloc_free_seq"):
         assert must in names
@@ -91,6 +92,56 @@ def test_write_and_copy_reject_bad_arguments(pa):
     assert L.pa_paged_kv_write(16, 16, 16, 0, 16, 16, 8, 16, 8, 128, 2, None) == 0  # nothing to do
     assert L.pa_copy_blocks(16, 16, 16, -1, 8, 16, 8, 128, 2, None) == -1
     assert L.pa_copy_blocks(16, 16, 16, 0, 8, 16, 8, 128, 2, None) == 0
+
+
+def _decode_fp8(pa, **kw):
+    args = dict(out=16, q=16, kc=16, vc=16, bt=16, mb=4, cl=16, B=2, H=8, Hk=2, D=128, bs=16, nb=64,
+                scale=0.1, ks=0.05, vs=0.05, maxctx=0, part=0, ws=None, wsb=0, dtype=2, stream=None)
+    args.update(kw)
+    a = args
+    return pa.lib().pa_paged_attention_decode_fp8(a["out"], a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["cl"],
+                                                  a["B"], a["H"], a["Hk"], a["D"], a["bs"], a["nb"], a["scale"],
+                                                  a["ks"], a["vs"], a["maxctx"], a["part"], a["ws"], a["wsb"],
+                                                  a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(dtype=0), -2),            # fp32 queries: not supported on the 8-bit path
+    (dict(dtype=3), -1),            # the storage code is not a query type
+    (dict(dtype=9), -1),
+    (dict(ks=0.0), -1),             # scales must be finite and positive
+    (dict(vs=-1.0), -1),
+    (dict(ks=float("inf")), -1),
+    (dict(vs=float("nan")), -1),
+    (dict(D=64), -2),               # head_dim 128 only
+    (dict(bs=4), -2),               # block size 8..128
+    (dict(bs=256), -2),
+    (dict(H=6, Hk=4), -1),
+    (dict(q=8), -1),
+])
+def test_decode_fp8_rejects_bad_arguments_on_the_host(pa, bad, code):
+    assert _decode_fp8(pa, **bad) == code
+
+
+def test_decode_fp8_with_no_sequences_is_a_no_op(pa):
+    assert _decode_fp8(pa, B=0) == 0
+
+
+def test_write_fp8_rejects_bad_arguments(pa):
+    L = pa.lib()
+    ok = dict(k=16, v=16, sm=16, T=4, kc=16, vc=16, nb=8, bs=16, hk=8, d=128, ks=0.1, vs=0.1, dt=2)
+
+    def w(**kw):
+        a = dict(ok, **kw)
+        return L.pa_paged_kv_write_fp8(a["k"], a["v"], a["sm"], a["T"], a["kc"], a["vc"], a["nb"], a["bs"],
+                                       a["hk"], a["d"], a["ks"], a["vs"], a["dt"], None)
+    assert w(dt=3) == -1                 # source must be fp32, fp16 or bf16
+    assert w(ks=0.0) == -1 and w(vs=float("inf")) == -1
+    assert w(hk=1, d=8) == -2            # rows of 8 codes: not a multiple of 16
+    assert w(T=0) == 0                   # nothing to do
+    assert w(k=8) == -1                  # misaligned
+    # copy_blocks takes the 8-bit storage code
+    assert L.pa_copy_blocks(16, 16, 16, 0, 8, 16, 8, 128, 3, None) == 0
 
 
 def test_get_device_error_requires_output_pointer(pa):

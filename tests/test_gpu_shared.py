@@ -102,6 +102,29 @@ def test_random_groups_against_oracle(pa, H, Hk, max_members, partition):
     assert np.abs(to_f64(plain) - to_f64(shared)).max() <= 2e-2
 
 
+@pytest.mark.parametrize("cut", [1, 5, 15, 16, 37])
+def test_prefix_lengths_off_block_boundaries(pa, cut):
+    """A caller may pass shared-prefix lengths that end inside a block (here the
+    groups' lengths minus `cut` tokens); the result is the same attention."""
+    groups = [(3, 5, 40), (8, 12, 300), (2, 3, 0)]
+    w = workloads.make_shared_groups(29 + cut, groups, 3, 32, 8, 128, 16, "bf16")
+    d = dev()
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    kc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=d)
+    vc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=d)
+    w.fill_cache_torch(kc, vc, include_newest=True)
+    q = w.q_values(like=kc).to(torch.bfloat16).contiguous()
+    pl, gm = pa.prefix_groups(w.block_tables, w.context_lens, w.block_size, 8)
+    pl = np.where(pl > 0, np.maximum(pl - cut, 1), 0).astype(np.int32)
+    out = torch.full_like(q, float("nan"))
+    pa.paged_attention_decode_shared(out, q, kc, vc, torch.as_tensor(w.block_tables, device=d),
+                                     torch.as_tensor(w.context_lens, device=d), torch.as_tensor(pl, device=d),
+                                     torch.as_tensor(gm, device=d), w.scale, max_prefix_len=int(pl.max()))
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    assert_close(to_f64(out), _oracle_full(w, np.arange(w.num_seqs)), "bf16", f"prefix cut {cut}")
+
+
 def test_no_groups_equals_plain_decode(pa):
     w = workloads.llama8b_decode(num_seqs=12)
     plain, shared, pl, gm = _run(pa, w, 8)

@@ -94,6 +94,36 @@ def content_rows(seed: int, tid: int, keys, positions, row_elems: int):
     return _irwin_hall(r[:, None] ^ ek[None, :])
 
 
+def content_codes(seed: int, tid: int, keys, positions, row_elems: int):
+    """Rows of 8-bit cache contents: OCP FP8 E4M3 codes drawn directly as bits.
+
+    Same keying as ``content_rows``; returns uint8 [n, row_elems]. Each code has a
+    random sign, a random 3-bit mantissa and an exponent field drawn uniformly
+    from {0 (subnormal), 4, 5, ..., 14}: magnitudes from 2^-9 to 240, never the
+    NaN pattern. With a scale of 5.625 / 448 the decoded values span about
+    [-3, 3], the range of the float rows. No quantisation is involved.
+    """
+    h = _mix_scalar(seed * 0x9E3779B1 + tid * 0x7FEB352D + 0x3C6EF372)
+    r = _mix32(((_mix32((keys + h) & M32)) + positions * 0x2C1B3C6D) & M32)
+    if _is_torch(keys):
+        import torch
+        e = torch.arange(row_elems, dtype=torch.int64, device=keys.device)
+    else:
+        e = np.arange(row_elems, dtype=np.int64)
+    ek = (e * 0x297A2D39) & M32
+    x = _mix32(r[:, None] ^ ek[None, :])
+    ex = ((x >> 8) & 0xFFFF) % 12
+    ex = ex + 3 * (ex > 0)                      # 0, or 4..14
+    code = ((x >> 31) << 7) | (ex << 3) | (x & 7)
+    if _is_torch(code):
+        import torch
+        return code.to(torch.uint8)
+    return code.astype(np.uint8)
+
+
+FP8_SCALE = 5.625 / 448.0     # float rows span [-5.625, 5.625]; that maps them onto [-448, 448]
+
+
 # ---------------------------------------------------------------------------
 # bf16 / f16 storage helpers (bit containers; values are already exact)
 # ---------------------------------------------------------------------------
@@ -194,6 +224,14 @@ class DecodeWorkload:
         keys = self.content_keys(seq_idx, positions)
         return content_rows(self.seed, tid, keys, positions, self.row_elems)
 
+    def kv_codes(self, tid: int, seq_idx, positions):
+        """uint8 [n, num_kv_heads*head_dim] E4M3 codes for an 8-bit cache."""
+        keys = self.content_keys(seq_idx, positions)
+        return content_codes(self.seed, tid, keys, positions, self.row_elems)
+
+    def _cache_rows(self, tid: int, seq_idx, positions, codes: bool):
+        return self.kv_codes(tid, seq_idx, positions) if codes else self.kv_rows(tid, seq_idx, positions)
+
     def q_values(self, like=None):
         """float32 [B, H, D] queries (q_mult applied; exact in every dtype)."""
         B, H, D = self.num_seqs, self.num_heads, self.head_dim
@@ -264,10 +302,12 @@ class DecodeWorkload:
 
     def fill_cache_torch(self, key_cache, value_cache, include_newest=False,
                          seqs=None, chunk_tokens=1 << 16):
-        """Write the pre-step contents into device (or host) torch caches.
+        """Write the pre-step contents into device (or host) torch caches; uint8
+        caches receive E4M3 codes (``kv_codes``), others float rows.
 
         Uses plain torch indexing; the library under test is not involved."""
         import torch
+        codes = key_cache.dtype == torch.uint8
         seqs = np.arange(self.num_seqs) if seqs is None else np.asarray(seqs)
         seq_idx, pos = self._positions(seqs, include_newest)
         slots = self._slots(seq_idx, pos)
@@ -278,8 +318,8 @@ class DecodeWorkload:
             si = torch.as_tensor(seq_idx[s:s + chunk_tokens], device=dev)
             pi = torch.as_tensor(pos[s:s + chunk_tokens], device=dev)
             sl = torch.as_tensor(slots[s:s + chunk_tokens], device=dev)
-            kflat[sl] = self.kv_rows(TID_K, si, pi).to(key_cache.dtype)
-            vflat[sl] = self.kv_rows(TID_V, si, pi).to(value_cache.dtype)
+            kflat[sl] = self._cache_rows(TID_K, si, pi, codes).to(key_cache.dtype)
+            vflat[sl] = self._cache_rows(TID_V, si, pi, codes).to(value_cache.dtype)
 
     def contiguous_kv(self, b: int, include_newest: bool = True):
         """float32 ([ctx, Hk, D], [ctx, Hk, D]) for sequence b, in position order."""
@@ -291,20 +331,22 @@ class DecodeWorkload:
         return (self.kv_rows(TID_K, seq_idx, pos).reshape(shp),
                 self.kv_rows(TID_V, seq_idx, pos).reshape(shp))
 
-    def _rows_host(self, seq_idx, pos):
-        """float32 numpy K and V rows, generated with torch's CPU threads."""
+    def _rows_host(self, seq_idx, pos, codes: bool = False):
+        """numpy K and V rows (float32, or uint8 codes), generated with torch's CPU threads."""
         import torch
         si = torch.from_numpy(np.ascontiguousarray(seq_idx))
         pi = torch.from_numpy(np.ascontiguousarray(pos))
-        return (self.kv_rows(TID_K, si, pi).numpy(), self.kv_rows(TID_V, si, pi).numpy())
+        return (self._cache_rows(TID_K, si, pi, codes).numpy(), self._cache_rows(TID_V, si, pi, codes).numpy())
 
-    def compact_host_view(self, seqs, rng_seed: int = 7, include_newest=False, chunk: int = 16384):
+    def compact_host_view(self, seqs, rng_seed: int = 7, include_newest=False, chunk: int = 16384,
+                          codes: bool = False):
         """A small host paged cache holding only ``seqs``.
 
         The chosen sequences' logical blocks are placed on a fresh random
         permutation of a pool just big enough for them. Returns a dict with
-        float32 caches, int32 block_tables/context_lens for the chosen rows and
-        the newest-token slots in the new pool."""
+        float32 caches (uint8 E4M3 codes when ``codes``), int32
+        block_tables/context_lens for the chosen rows and the newest-token slots
+        in the new pool."""
         seqs = np.asarray(seqs, dtype=np.int64)
         bs = self.block_size
         ctx = self.context_lens.astype(np.int64)[seqs]
@@ -318,7 +360,7 @@ class DecodeWorkload:
             tables[i, :n] = perm[off:off + n]
             off += n
         nblk = max(total, 1)
-        kc = np.zeros((nblk, bs, self.num_kv_heads, self.head_dim), np.float32)
+        kc = np.zeros((nblk, bs, self.num_kv_heads, self.head_dim), np.uint8 if codes else np.float32)
         vc = np.zeros_like(kc)
         kflat = kc.reshape(-1, self.row_elems)
         vflat = vc.reshape(-1, self.row_elems)
@@ -328,7 +370,7 @@ class DecodeWorkload:
             for s in range(0, n, chunk):
                 p = np.arange(s, min(n, s + chunk), dtype=np.int64)
                 slot = tables[i, p // bs].astype(np.int64) * bs + p % bs
-                k, v = self._rows_host(np.full(p.shape[0], int(b), np.int64), p)
+                k, v = self._rows_host(np.full(p.shape[0], int(b), np.int64), p, codes)
                 kflat[slot] = k
                 vflat[slot] = v
         newest = np.full(seqs.shape[0], -1, np.int32)
@@ -339,16 +381,18 @@ class DecodeWorkload:
                     context_lens=ctx.astype(np.int32), slot_mapping=newest,
                     num_blocks=nblk)
 
-    def algorithmic_bytes(self) -> dict:
+    def algorithmic_bytes(self, cache_elem_bytes: int | None = None) -> dict:
         """Bytes a decode step must move at minimum (K and V once per (seq, kv-head),
-        q in, out back, the table entries used and the lengths)."""
+        q in, out back, the table entries used and the lengths). cache_elem_bytes:
+        size of a cache element when it differs from the dtype's (1 for 8-bit)."""
         s = {"f32": 4, "f16": 2, "bf16": 2}[self.dtype]
+        c = s if cache_elem_bytes is None else cache_elem_bytes
         ctx = self.context_lens.astype(np.int64)
         nb = (ctx + self.block_size - 1) // self.block_size
-        kv = int(ctx.sum()) * self.num_kv_heads * self.head_dim * 2 * s
+        kv = int(ctx.sum()) * self.num_kv_heads * self.head_dim * 2 * c
         qo = 2 * self.num_seqs * self.num_heads * self.head_dim * s
         meta = 4 * int(nb.sum()) + 4 * self.num_seqs
-        write = 2 * int((ctx > 0).sum()) * self.row_elems * s * 2 + 4 * self.num_seqs
+        write = 2 * int((ctx > 0).sum()) * self.row_elems * (s + c) + 4 * self.num_seqs
         return dict(kv=kv, qo=qo, meta=meta, decode=kv + qo + meta, write=write)
 
 
