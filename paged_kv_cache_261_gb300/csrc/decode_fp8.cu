@@ -100,11 +100,12 @@ constexpr int kBarVbFree = kBarVbFull + 2;                    // [2]
 constexpr int kBarFullV = kBarVbFree + 2;                     // [kStages]
 constexpr int kNumBars = kBarFullV + kStages;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;              // tmem base, abort flag, 2 item counts
-constexpr int kOffPrefix = kOffMisc + 32;                     // int [kMaxSeqs + 1]
+constexpr int kOffPrefix = (kOffMisc + 32 + 15) & ~15;        // int [kMaxSeqs + 1]; later the item table
 constexpr int kOffOrder = kOffPrefix + (kMaxSeqs + 1) * 4;    // int [kMaxSeqs]
 constexpr int kOffCtx = kOffOrder + kMaxSeqs * 4;             // int [kMaxSeqs] clamped context lengths
 constexpr int kOffPs = kOffCtx + kMaxSeqs * 4;                // int [kMaxSeqs] first token of this pass
 constexpr int kSmemUsed = kOffPs + kMaxSeqs * 4;
+static_assert(kSmemUsed - kOffPrefix >= decode_order::kTableItems * 16, "item table fits the ordering arrays");
 constexpr int kSmemBytes = kSmemUsed + 1024;                  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kStageBytes % 1024 == 0 && kOffVb % 1024 == 0 && kOffP % 1024 == 0,
@@ -327,6 +328,11 @@ __global__ __launch_bounds__(threads_for(GT), 1) void decode_fp8_kernel(const __
     const uint32_t tmem = *tmem_slot;
     const int n4 = counts[0];
     const int total_items = (counts[0] + counts[1]) * p.num_kv_heads;
+    // this CTA's item descriptors, computed once and kept over the ordering arrays
+    int4 *items = reinterpret_cast<int4 *>(smem + kOffPrefix);
+    decode_order::build_item_table<(decode_order::kTableItems + threads_for(GT) - 1) / threads_for(GT)>(p, prefix, order, n4, cache, total_items, items);
+    const int nmy = decode_order::cta_items(total_items);
+    __syncthreads();
 
     if (warp == 0 || warp == kVProdWarp) {
         // ------------------------------------------------------------ producers
@@ -338,8 +344,8 @@ __global__ __launch_bounds__(threads_for(GT), 1) void decode_fp8_kernel(const __
         const int nbt = kTile / p.block_size;       // physical blocks per tile
         uint32_t it = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-            const Item I = get_item(idx, prefix, order, n4, p, cache);
+        for (int k = 0; k < nmy && ok; ++k) {
+            const Item I = decode_order::unpack_item(items[k]);
             const decode_order::ItemTable tb = decode_order::load_item_table(p, I, lane);
             const int qrow = I.b * p.num_heads + I.kvh * G;
             for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
@@ -389,8 +395,8 @@ __global__ __launch_bounds__(threads_for(GT), 1) void decode_fp8_kernel(const __
             const uint32_t s80 = smem_addr(s8);
             uint32_t it = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-                const Item I = get_item(idx, prefix, order, n4, p, cache);
+            for (int k = 0; k < nmy && ok; ++k) {
+                const Item I = decode_order::unpack_item(items[k]);
                 for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
                     const int stage = it % kStages, buf = it & 1;
                     if (*abort_flag || !mbar_wait(&bars.full[stage], (it / kStages) & 1) ||
@@ -427,8 +433,8 @@ __global__ __launch_bounds__(threads_for(GT), 1) void decode_fp8_kernel(const __
             const uint32_t sVb0 = smem_addr(sVb), sP0 = smem_addr(sP);
             uint32_t it = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-                const Item I = get_item(idx, prefix, order, n4, p, cache);
+            for (int k = 0; k < nmy && ok; ++k) {
+                const Item I = decode_order::unpack_item(items[k]);
                 for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
                     const int buf = it & 1;
                     const uint32_t bph = (it >> 1) & 1;
@@ -464,8 +470,8 @@ __global__ __launch_bounds__(threads_for(GT), 1) void decode_fp8_kernel(const __
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         uint32_t it = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-            const Item I = get_item(idx, prefix, order, n4, p, cache);
+        for (int k = 0; k < nmy && ok; ++k) {
+            const Item I = decode_order::unpack_item(items[k]);
             for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
                 const int stage = it % kStages, buf = it & 1;
                 uint64_t *free_bar = is_k ? &bars.kb_free[buf] : &bars.vb_free[buf];
@@ -518,8 +524,8 @@ __global__ __launch_bounds__(threads_for(GT), 1) void decode_fp8_kernel(const __
             }
             return true;
         };
-        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-            const Item I = get_item(idx, prefix, order, n4, p, cache);
+        for (int k = 0; k < nmy && ok; ++k) {
+            const Item I = decode_order::unpack_item(items[k]);
             for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
                 const int stage = it % kStages, buf = it & 1;
                 if (__any_sync(0xffffffffu, *abort_flag != 0) ||
@@ -553,8 +559,8 @@ __global__ __launch_bounds__(threads_for(GT), 1) void decode_fp8_kernel(const __
         uint32_t it = 0, nfin = 0;
         bool ok = true;
         float m_run[GT], l_part[GT], o_acc[GT], alpha_prev[GT];
-        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-            const Item I = get_item(idx, prefix, order, n4, p, cache);
+        for (int k = 0; k < nmy && ok; ++k) {
+            const Item I = decode_order::unpack_item(items[k]);
             const int64_t head0 = (int64_t)I.b * p.num_heads + (int64_t)I.kvh * G;
             if (I.ntiles == 0) {
 #pragma unroll
@@ -761,10 +767,19 @@ bool decode_fp8_supported(const DecodeParams &p, int dtype) {
 // Batches above kMaxSeqs sequences run as independent launches of up to kMaxSeqs.
 int launch_decode_fp8(const DecodeParams &p, float v_scale, int dtype, cudaStream_t stream) {
     if (!decode_fp8_supported(p, dtype)) return -2;
-    for (int b0 = 0; b0 < p.num_seqs; b0 += kMaxSeqs) {
+    // sequences per launch: at most kMaxSeqs, and few enough that no CTA gets more
+    // than the item table holds (items <= num_seqs * kv heads * partitions)
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -1;
+    const int64_t per_seq = (int64_t)p.num_kv_heads * p.max_partitions;
+    const int64_t by_items = (int64_t)decode_order::kTableItems * sms / (per_seq > 0 ? per_seq : 1);
+    const int chunk = (int)(by_items < 1 ? 1 : (by_items < kMaxSeqs ? by_items : kMaxSeqs));
+    for (int b0 = 0; b0 < p.num_seqs; b0 += chunk) {
         DecodeParams c = p;
         const int64_t rows = (int64_t)b0 * p.num_heads;
-        c.num_seqs = min(kMaxSeqs, p.num_seqs - b0);
+        c.num_seqs = min(chunk, p.num_seqs - b0);
         c.q = static_cast<const char *>(p.q) + rows * kD * 2;
         c.out = static_cast<char *>(p.out) + rows * kD * 2;
         c.block_tables = p.block_tables + (int64_t)b0 * p.max_blocks_per_seq;

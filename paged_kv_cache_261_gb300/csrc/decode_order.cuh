@@ -144,6 +144,56 @@ __device__ __forceinline__ void build(const DecodeParams &p, int *prefix, int *o
     }
 }
 
+// ---- per-CTA item table ----------------------------------------------------------
+// A CTA works on items blockIdx.x, blockIdx.x + gridDim.x, ...; its k-th item's
+// descriptor is computed once, in parallel, and kept in shared memory (16 bytes),
+// so no role repeats the search and the divisions of get_item at every item.
+constexpr int kTableItems = 512;       // items per CTA the table holds (8 KiB)
+
+__device__ __forceinline__ int4 pack_item(const Item &it) {
+    return make_int4(it.b | (it.kvh << 16), it.t0, it.t1, it.slot | (it.direct ? int(0x80000000u) : 0));
+}
+__device__ __forceinline__ Item unpack_item(int4 d) {
+    Item it;
+    it.b = d.x & 0xFFFF;
+    it.kvh = (int)((unsigned)d.x >> 16);
+    it.t0 = d.y;
+    it.t1 = d.z;
+    it.slot = d.w & 0x7FFFFFFF;
+    it.direct = d.w < 0;
+    it.part = 0;                     // not needed once the table is built
+    it.ntiles = it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
+    return it;
+}
+// Items of this CTA. The host sizes launches so that this never exceeds
+// kTableItems; the clamp only keeps every table access inside the table.
+__device__ __forceinline__ int cta_items(int total_items) {
+    const int n = total_items > (int)blockIdx.x
+                      ? (total_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                      : 0;
+    return n < kTableItems ? n : kTableItems;
+}
+// Every thread of the CTA calls this after build() and a barrier. The table is
+// written over `area` (the ordering arrays, no longer needed) once every thread
+// has computed its descriptors; the caller synchronises before reading it.
+template <int kPerThread>
+__device__ __forceinline__ void build_item_table(const DecodeParams &p, const int *prefix, const int *order,
+                                                 int n4, const SeqCache &c, int total_items, int4 *area) {
+    const int n = cta_items(total_items);
+    int4 d[kPerThread];
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+        const int k = (int)threadIdx.x + u * (int)blockDim.x;
+        if (k < n) d[u] = pack_item(get_item((int)blockIdx.x + k * (int)gridDim.x, prefix, order, n4, p, c));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+        const int k = (int)threadIdx.x + u * (int)blockDim.x;
+        if (k < n) area[k] = d[u];
+    }
+}
+
 // Block-table entries of one item, read once with one coalesced load per 32
 // blocks: entry j (the item's j-th block) sits in register j / 32 of lane
 // j % 32. Items of up to kCachedBlocks blocks (every item of a 512-token
