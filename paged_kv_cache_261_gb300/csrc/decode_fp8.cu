@@ -64,7 +64,6 @@ constexpr int kStageBytes = 2 * kTile8Bytes + kQBytes;
 constexpr int kChunkBytes = kTile * 128;          // 128 rows x 64 dims x 2 B
 constexpr int kKVBytes = 2 * kChunkBytes;         // one 16-bit tile, both 64-dim halves
 constexpr int kPBytes = 2 * kN * 128;             // P^T: 16 rows x 128 tokens
-constexpr int kSoftmaxThreads = 128;
 constexpr int kConvWarp0 = 7;                     // first converter warp
 // Converter warps: 8 (one warpgroup for K, one for V) where the softmax warps'
 // registers allow it (up to 8 query heads per kv head), else 4 doing both.
@@ -81,8 +80,8 @@ constexpr int kOff8 = 0;                                      // [kStages] x {K 
 constexpr int kOffVb = kOff8 + kStages * kStageBytes;         // two 16-bit V tiles
 constexpr int kOffP = kOffVb + 2 * kKVBytes;
 constexpr int kOffRed = kOffP + 2 * kPBytes;                  // float [2][4][16]
-constexpr int kOffLRed = kOffRed + 2 * 4 * kN * 4;            // float [4][16]
-constexpr int kOffBar = kOffLRed + 4 * kN * 4;
+constexpr int kOffLRed = kOffRed + 2 * 4 * kN * 4;            // float [2][4][16] (by item parity)
+constexpr int kOffBar = kOffLRed + 2 * 4 * kN * 4;
 // mbarrier slots, in order; kNumBars counts them
 constexpr int kBarFull = 0;                                   // [kStages]
 constexpr int kBarEmpty = kBarFull + kStages;                 // [kStages]
@@ -294,13 +293,13 @@ __global__ __launch_bounds__(threads_for(GT), 1) void decode_fp8_kernel(const __
             mbar_init(&bars.p_full[i], 4);
             mbar_init(&bars.o_full[i], 1);
             mbar_init(&bars.o_free[i], 4);
-            mbar_init(&bars.red[i], kSoftmaxThreads);
+            mbar_init(&bars.red[i], 4);          // one arrival per softmax warp
             mbar_init(&bars.vb_full[i], 4);
             mbar_init(&bars.vb_free[i], 1);
             mbar_init(&bars.kb_full[i], 4);
             mbar_init(&bars.kb_free[i], 1);
         }
-        mbar_init(bars.fin, kSoftmaxThreads);
+        mbar_init(bars.fin, 4);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -610,7 +609,8 @@ __global__ __launch_bounds__(threads_for(GT), 1) void decode_fp8_kernel(const __
                     const float mx = warp_max(s[g]);
                     if (lane == 0) rd[q4 * kN + g] = mx;
                 }
-                mbar_arrive(&bars.red[it & 1]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.red[it & 1]);
                 if (!warp_wait(&bars.red[it & 1], (it >> 1) & 1)) {
                     ok = false;
                     break;
@@ -644,24 +644,23 @@ __global__ __launch_bounds__(threads_for(GT), 1) void decode_fp8_kernel(const __
                 ok = false;
                 break;
             }
+            // ---- finalize the item: sum of the token lanes' partial l per head
+            // (lred is double-buffered by item parity: one barrier per item)
+            float *lr = lred + (nfin & 1) * 4 * kN;
 #pragma unroll
             for (int g = 0; g < GT; ++g) {
                 const float ls = warp_sum(l_part[g]);
-                if (lane == 0) lred[q4 * kN + g] = ls;
+                if (lane == 0) lr[q4 * kN + g] = ls;
             }
-            mbar_arrive(bars.fin);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.fin);
             if (!warp_wait(bars.fin, nfin++ & 1)) {
                 ok = false;
                 break;
             }
             float l_tot[GT];
 #pragma unroll
-            for (int g = 0; g < GT; ++g) l_tot[g] = lred[g] + lred[kN + g] + lred[2 * kN + g] + lred[3 * kN + g];
-            mbar_arrive(bars.fin);                    // lred may be rewritten after this phase
-            if (!warp_wait(bars.fin, nfin++ & 1)) {
-                ok = false;
-                break;
-            }
+            for (int g = 0; g < GT; ++g) l_tot[g] = lr[g] + lr[kN + g] + lr[2 * kN + g] + lr[3 * kN + g];
             if (I.direct) {
 #pragma unroll
                 for (int g = 0; g < GT; ++g)

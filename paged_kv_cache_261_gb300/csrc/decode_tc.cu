@@ -69,7 +69,6 @@ constexpr int kPBytes = 2 * kN * 128;             // P^T: 16 rows x 128 tokens
 constexpr int kThreads = 288;
 constexpr int kVProdWarp = 7;                     // issues the V boxes
 constexpr int kPvWarp = 8;                        // issues the P.V MMAs
-constexpr int kSoftmaxThreads = 128;
 constexpr int kMaxSeqs = 512;                     // sequences per launch (the host splits larger batches)
 constexpr uint32_t kTmemCols = 64;                // S[2] x 16 + O[2] x 16 columns
 constexpr int kPrefetchTiles = 2;                 // L2 prefetch distance, in tiles, ahead of the loads
@@ -80,8 +79,8 @@ constexpr int kOffV = kOffK + kStages * kKVBytes;
 constexpr int kOffQ = kOffV + kStages * kKVBytes;
 constexpr int kOffP = kOffQ + kStages * kQBytes;
 constexpr int kOffRed = kOffP + 2 * kPBytes;                  // float [2][4][16]
-constexpr int kOffLRed = kOffRed + 2 * 4 * kN * 4;            // float [4][16]
-constexpr int kOffBar = kOffLRed + 4 * kN * 4;                // uint64 barriers
+constexpr int kOffLRed = kOffRed + 2 * 4 * kN * 4;            // float [2][4][16] (by item parity)
+constexpr int kOffBar = kOffLRed + 2 * 4 * kN * 4;                // uint64 barriers
 // mbarrier slots, in order; kNumBars counts them
 constexpr int kBarFull = 0;                                   // [kStages] K and Q of the stage landed
 constexpr int kBarEmpty = kBarFull + kStages;                 // [kStages]
@@ -189,9 +188,9 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             mbar_init(&bars.p_full[i], 4);
             mbar_init(&bars.o_full[i], 1);
             mbar_init(&bars.o_free[i], 4);
-            mbar_init(&bars.red[i], kSoftmaxThreads);
+            mbar_init(&bars.red[i], 4);          // one arrival per softmax warp
         }
-        mbar_init(bars.fin, kSoftmaxThreads);
+        mbar_init(bars.fin, 4);
         *abort_flag = 0;
         *loads_issued = 0;
         mbar_fence_init();
@@ -457,7 +456,8 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                     const float mx = warp_max(s[g]);
                     if (lane == 0) rd[q4 * kN + g] = mx;
                 }
-                mbar_arrive(&bars.red[it & 1]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.red[it & 1]);
                 if (!warp_wait(&bars.red[it & 1], (it >> 1) & 1)) {
                     ok = false;
                     break;
@@ -508,24 +508,22 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                 break;
             }
             // ---- finalize the item: sum of the token lanes' partial l per head
+            // (lred is double-buffered by item parity: one barrier per item)
+            float *lr = lred + (nfin & 1) * 4 * kN;
 #pragma unroll
             for (int g = 0; g < GT; ++g) {
                 const float ls = warp_sum(l_part[g]);
-                if (lane == 0) lred[q4 * kN + g] = ls;
+                if (lane == 0) lr[q4 * kN + g] = ls;
             }
-            mbar_arrive(bars.fin);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.fin);
             if (!warp_wait(bars.fin, nfin++ & 1)) {
                 ok = false;
                 break;
             }
             float l_tot[GT];
 #pragma unroll
-            for (int g = 0; g < GT; ++g) l_tot[g] = lred[g] + lred[kN + g] + lred[2 * kN + g] + lred[3 * kN + g];
-            mbar_arrive(bars.fin);                    // lred may be rewritten after this phase
-            if (!warp_wait(bars.fin, nfin++ & 1)) {
-                ok = false;
-                break;
-            }
+            for (int g = 0; g < GT; ++g) l_tot[g] = lr[g] + lr[kN + g] + lr[2 * kN + g] + lr[3 * kN + g];
             if (I.direct) {
 #pragma unroll
                 for (int g = 0; g < GT; ++g)
