@@ -19,13 +19,16 @@
 // rescaled (tcgen05.ld / st of the row) only when a row's max grows by more than
 // 2^8, otherwise the stale reference max is kept (the final O / l is the same).
 //
-// Roles (192 threads, one persistent CTA per SM):
+// Roles (224 threads, one persistent CTA per SM):
 //   warp 0     TMA: the item's query rows (3-D map over [tokens, heads, dims]),
-//              then per key tile the K/V boxes of each physical block through
-//              the block table into 2-stage K and V rings with separate
-//              barriers (K freed after its S MMA, V after its P.V MMA; each
-//              tile's V is issued after the next tile's K); blocks past the
-//              last visible key load from an out-of-range coordinate (zeros).
+//              then per key tile the K boxes of each physical block into a
+//              2-stage K ring.
+//   warp 6     TMA: the V boxes of every key tile into a 2-stage V ring with its
+//              own barriers (K freed after its S MMA, V after its P.V MMA). Each
+//              producer reads an item's block ids once, coalesced, at item start;
+//              blocks past the last visible key load from an out-of-range
+//              coordinate (zeros). With one producer warp for both operands the
+//              producer was busy 95 % of the time and the MMA waited on K.
 //   warp 1     one thread issues the MMAs and owns tensor memory.
 //   warps 2-5  softmax (scale, causal mask, exp2, P to shared memory, V rows of
 //              keys past the last visible one zeroed) and the epilogue O / l.
@@ -55,8 +58,8 @@ constexpr int kChunk = 128 * 128;              // 128 rows x 128 bytes (one 64-e
 constexpr int kKVBytes = 2 * kChunk;           // one K (or V) tile
 constexpr int kQBytes = 2 * kChunk;
 constexpr int kPBytes = 2 * kChunk;
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 224;                  // + warp 6: V producer
+constexpr int kVProdWarp = 6;
 constexpr uint32_t kTmemCols = 512;            // S[2] x 128 + O x 128 (+ spare)
 constexpr uint32_t kColO = 2 * kKT;
 constexpr float kRescaleLog2 = 8.f;            // keep the reference max until a row's max grows by 2^8
@@ -129,6 +132,51 @@ __device__ __forceinline__ bool get_gitem(int idx, const PrefillParams &p, PItem
     it.q_row0 = 0;
     it.nq = n;
     return true;
+}
+
+// Block-table entries of an item's keys, read once at item start with one
+// coalesced load per 32 blocks: entry j (the item's j-th block from key0) sits in
+// register j / 32 of lane j % 32. Items of up to kCachedBlocks blocks are served
+// from registers; entries past that are read per tile.
+constexpr int kCachedBlocks = 256;
+struct KeyTable {
+    const int32_t *row;
+    int nblk;
+    int e[kCachedBlocks / 32];
+};
+__device__ __forceinline__ KeyTable load_key_table(const PrefillParams &p, const PItem &I, int lane) {
+    KeyTable t;
+    t.row = p.block_tables + (int64_t)I.b * p.max_blocks_per_seq + (I.key0 >> p.log2_block_size);
+    t.nblk = I.kmax > I.key0 ? (I.kmax - I.key0 + p.block_size - 1) >> p.log2_block_size : 0;
+#pragma unroll
+    for (int k = 0; k < kCachedBlocks / 32; ++k) {
+        const int j = k * 32 + lane;
+        t.e[k] = j < t.nblk ? t.row[j] : -1;
+    }
+    return t;
+}
+// Physical block of block `lane` of key tile `tile` (nbt blocks per tile; nbt
+// divides 32), or num_blocks (TMA fills zeros) past the item's keys or for a bad
+// id (reported when `report`). Every lane of the warp calls this.
+__device__ __forceinline__ int tile_block(const KeyTable &t, const PrefillParams &p, int tile, int nbt, int lane,
+                                          bool report) {
+    const int j0 = tile * nbt, j = j0 + lane;
+    const bool live = lane < nbt && j < t.nblk;
+    const int k = j0 >> 5;
+    int e;
+    if (k < kCachedBlocks / 32) {
+        int v = t.e[0];
+#pragma unroll
+        for (int i = 1; i < kCachedBlocks / 32; ++i)
+            if (k == i) v = t.e[i];
+        e = __shfl_sync(0xffffffffu, v, j & 31);
+    } else {
+        e = live ? t.row[j] : -1;
+    }
+    if (!live) return (int)p.num_blocks;
+    if (e >= 0 && e < p.num_blocks) return e;
+    if (report) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+    return (int)p.num_blocks;
 }
 
 template <typename T>
@@ -209,38 +257,16 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        // Per item: the query rows, then per key tile its K, with each tile's V
-        // issued after the next tile's K (K is needed a step earlier than V).
+        // ------------------------------------------------------------ TMA producer: Q and K
+        // Per item: the query rows, then per key tile its K boxes. The item's block
+        // ids are read once at item start.
         const int nbt = kKT / p.block_size;
-        uint32_t it = 0, n = 0, nv = 0;                 // K tiles, items, V tiles issued
-        bool ok = true, v_pending = false;
-        int v_phys = 0, v_kvh = 0;
-        auto issue_v = [&]() -> bool {                  // V of tile nv (block ids saved with its K)
-            const int stage = nv & 1;
-            int w = 1;
-            if (lane == 0) w = mbar_wait(&v_empty[stage], ((nv >> 1) & 1) ^ 1) ? 1 : 0;
-            w = __shfl_sync(0xffffffffu, w, 0);
-            if (!w) return false;
-            if (lane == 0) mbar_arrive_expect_tx(&v_full[stage], kKVBytes);
-            __syncwarp();
-            if (lane < nbt) {
-                unsigned char *dv = sV + stage * kKVBytes + lane * p.block_size * 128;
-                tma_load_4d(dv, &tm_v, &v_full[stage], 0, v_kvh, 0, v_phys);
-                tma_load_4d(dv + kChunk, &tm_v, &v_full[stage], 64, v_kvh, 0, v_phys);
-            }
-            ++nv;
-            v_pending = false;
-            return true;
-        };
+        uint32_t it = 0, n = 0;                         // K tiles, items issued
+        bool ok = true;
         for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
             PItem I;
             if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
-            if (v_pending && !issue_v()) {
-                ok = false;
-                break;
-            }
-            const int32_t *table = p.block_tables + (int64_t)I.b * p.max_blocks_per_seq;
+            const KeyTable tb = load_key_table(p, I, lane);
             int w = 1;
             if (lane == 0) {
                 w = mbar_wait(q_empty, (n & 1) ^ 1) ? 1 : 0;
@@ -269,15 +295,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
             ++n;
             for (int j = 0; j < I.ntiles; ++j, ++it) {
                 const int stage = it & 1;
-                int phys = (int)p.num_blocks;
-                if (lane < nbt) {
-                    const int tok = I.key0 + j * kKT + lane * p.block_size;
-                    if (tok < I.kmax) {
-                        const int e = table[tok >> p.log2_block_size];
-                        if (e >= 0 && e < p.num_blocks) phys = e;
-                        else raise_error(p.err, PA_DEVERR_BLOCK_ID);
-                    }
-                }
+                const int phys = tile_block(tb, p, j, nbt, lane, true);
                 if (lane == 0) w = mbar_wait(&k_empty[stage], ((it >> 1) & 1) ^ 1) ? 1 : 0;
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (!w || *abort_flag) {
@@ -291,25 +309,50 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                     tma_load_4d(dk, &tm_k, &k_full[stage], 0, I.kvh, 0, phys);
                     tma_load_4d(dk + kChunk, &tm_k, &k_full[stage], 64, I.kvh, 0, phys);
                 }
-                if (v_pending && !issue_v()) {
-                    ok = false;
-                    break;
-                }
-                v_pending = true;
-                v_phys = phys;
-                v_kvh = I.kvh;
             }
         }
-        if (ok && v_pending && !issue_v()) ok = false;
         if (!ok) {
             *abort_flag = 1;
             raise_error(p.err, PA_DEVERR_WAIT);
         }
         if (lane == 0) {   // drain copies in flight
             for (uint32_t j = it > 2u ? it - 2 : 0; j < it; ++j) mbar_wait(&k_full[j & 1], (j >> 1) & 1);
-            for (uint32_t j = nv > 2u ? nv - 2 : 0; j < nv; ++j) mbar_wait(&v_full[j & 1], (j >> 1) & 1);
             if (n > 0) mbar_wait(q_full, (n - 1) & 1);
         }
+    } else if (warp == kVProdWarp) {
+        // ------------------------------------------------------------ TMA producer: V
+        const int nbt = kKT / p.block_size;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+            PItem I;
+            if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
+            const KeyTable tb = load_key_table(p, I, lane);
+            for (int j = 0; j < I.ntiles; ++j, ++it) {
+                const int stage = it & 1;
+                const int phys = tile_block(tb, p, j, nbt, lane, false);
+                int w = 1;
+                if (lane == 0) w = mbar_wait(&v_empty[stage], ((it >> 1) & 1) ^ 1) ? 1 : 0;
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&v_full[stage], kKVBytes);
+                __syncwarp();
+                if (lane < nbt) {
+                    unsigned char *dv = sV + stage * kKVBytes + lane * p.block_size * 128;
+                    tma_load_4d(dv, &tm_v, &v_full[stage], 0, I.kvh, 0, phys);
+                    tma_load_4d(dv + kChunk, &tm_v, &v_full[stage], 64, I.kvh, 0, phys);
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            raise_error(p.err, PA_DEVERR_WAIT);
+        }
+        if (lane == 0)
+            for (uint32_t j = it > 2u ? it - 2 : 0; j < it; ++j) mbar_wait(&v_full[j & 1], (j >> 1) & 1);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -379,7 +422,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // ------------------------------------------------------------ softmax / epilogue
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;                 // MMA row of this thread (and key row for V zeroing)
