@@ -13,8 +13,11 @@
 // rows are (query token, head of the group) pairs: QT = 128 / Gp tokens x Gp
 // heads, Gp = G rounded up to a power of two. Per tile of 128 keys:
 //   S[128 rows x 128 keys] = Q . K^T    (tcgen05 kind::f16, M=128 N=128 K=128)
-//   O[128 rows x 128 dims] += P . V     (P from shared memory, V MN-major)
-// S is double-buffered and O stays in tensor memory (384 of 512 columns).
+//   O[128 rows x 128 dims] += P . V     (P from tensor memory, V MN-major)
+// S is double-buffered and O stays in tensor memory; P is written by the softmax
+// threads into tensor memory (each thread's row is its lane: 16-bit pairs, two
+// 64-column buffers), where the P.V MMA takes its A operand -- no shared-memory
+// round trip for P (all 512 columns in use).
 // Thread = row for the softmax, so the max and the sum are thread-local; O is
 // rescaled (tcgen05.ld / st of the row) only when a row's max grows by more than
 // 2^8, otherwise the stale reference max is kept (the final O / l is the same).
@@ -30,7 +33,7 @@
 //              coordinate (zeros). With one producer warp for both operands the
 //              producer was busy 95 % of the time and the MMA waited on K.
 //   warp 1     one thread issues the MMAs and owns tensor memory.
-//   warps 2-5  softmax (scale, causal mask, exp2, P to shared memory, V rows of
+//   warps 2-5  softmax (scale, causal mask, exp2, P to tensor memory, V rows of
 //              keys past the last visible one zeroed) and the epilogue O / l.
 // Items are ordered with the query tiles of one (sequence, kv head) adjacent,
 // so the CTAs working on them at the same time share its K/V through L2.
@@ -60,15 +63,16 @@ constexpr int kQBytes = 2 * kChunk;
 constexpr int kPBytes = 2 * kChunk;
 constexpr int kThreads = 224;                  // + warp 6: V producer
 constexpr int kVProdWarp = 6;
-constexpr uint32_t kTmemCols = 512;            // S[2] x 128 + O x 128 (+ spare)
+constexpr uint32_t kTmemCols = 512;            // S[2] x 128 + O x 128 + P[2] x 64
 constexpr uint32_t kColO = 2 * kKT;
+constexpr uint32_t kColP = 3 * kKT;            // P[2]: 64 columns each, 16-bit pairs per lane (row)
 constexpr float kRescaleLog2 = 8.f;            // keep the reference max until a row's max grows by 2^8
 
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kStages * kKVBytes;
 constexpr int kOffQ = kOffV + kStages * kKVBytes;
 constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kOffBar = kOffP;
 constexpr int kNumBars = 19;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 16;
@@ -179,6 +183,15 @@ __device__ __forceinline__ int tile_block(const KeyTable &t, const PrefillParams
     return (int)p.num_blocks;
 }
 
+// D (tmem) [+]= A (tmem: M rows in lanes, 16-bit K pairs per column) * B (smem desc).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::
+            "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     if constexpr (std::is_same<T, __nv_bfloat16>::value) {
@@ -210,7 +223,6 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
     unsigned char *sK = smem + kOffK;
     unsigned char *sV = smem + kOffV;
     unsigned char *sQ = smem + kOffQ;
-    unsigned char *sP = smem + kOffP;
     uint64_t *bb = reinterpret_cast<uint64_t *>(smem + kOffBar);
     // K and V stages have separate barriers: a K stage is free again as soon as its
     // S MMA is done, a V stage only after its P.V MMA.
@@ -359,7 +371,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
             constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
             const uint32_t idesc_s = instr_desc_f16(kRows, kKT, kBf16, false, false);
             const uint32_t idesc_o = instr_desc_f16(kRows, kD, kBf16, false, true);
-            const uint32_t sK0 = smem_addr(sK), sV0 = smem_addr(sV), sQ0 = smem_addr(sQ), sP0 = smem_addr(sP);
+            const uint32_t sK0 = smem_addr(sK), sV0 = smem_addr(sV), sQ0 = smem_addr(sQ);
             uint32_t it = 0, n = 0;
             bool ok = true;
             // O += P(j) V(j); `first` starts the item's accumulator
@@ -368,12 +380,12 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                 if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1)) return false;
                 if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1)) return false;
                 tc_fence_after();
-                const uint32_t vb = sV0 + (j & 1) * kKVBytes, pb = sP0 + (j & 1) * kPBytes;
+                const uint32_t vb = sV0 + (j & 1) * kKVBytes;
 #pragma unroll
                 for (int kk = 0; kk < kKT / 16; ++kk) {
-                    const uint64_t a = smem_desc(pb + (kk >> 2) * kChunk + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = smem_desc(vb + kk * 2048, kChunk, 1024);
-                    mma_f16(tmem + kColO, a, b, idesc_o, (first && kk == 0) ? 0u : 1u);
+                    mma_f16_tmem_a(tmem + kColO, tmem + kColP + (j & 1) * 64 + kk * 8, b, idesc_o,
+                                   (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(&o_done[j & 1]);
                 mma_commit(&v_empty[j & 1]);
@@ -499,28 +511,28 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                     ok = false;
                     break;
                 }
-                unsigned char *prow = sP + buf * kPBytes + r * 128;
+                tc_fence_after();
                 const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;    // rows with no visible key: p = 0
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int u = 0; u < kKT / 8; ++u) {
-                    float pv[8];
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pw[32];                  // keys 64h .. 64h + 63 as 16-bit pairs
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) pv[e] = fast_exp2(fmaf(__uint_as_float(sr[u * 8 + e]), p.scale_log2, neg_m));
-                    uint4 pk;
-                    pk.x = pack2<T>(pv[0], pv[1]);
-                    pk.y = pack2<T>(pv[2], pv[3]);
-                    pk.z = pack2<T>(pv[4], pv[5]);
-                    pk.w = pack2<T>(pv[6], pv[7]);
-                    const float2 a0 = unpack2<T>(pk.x), a1 = unpack2<T>(pk.y);
-                    const float2 a2 = unpack2<T>(pk.z), a3 = unpack2<T>(pk.w);
-                    ls[0] += a0.x + a0.y;
-                    ls[1] += a1.x + a1.y;
-                    ls[2] += a2.x + a2.y;
-                    ls[3] += a3.x + a3.y;
-                    const int chunk = u >> 3, unit = (u & 7) ^ (r & 7);
-                    *reinterpret_cast<uint4 *>(prow + chunk * kChunk + unit * 16) = pk;
+                    for (int u = 0; u < 8; ++u) {
+                        float pv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            pv[e] = fast_exp2(fmaf(__uint_as_float(sr[h * 64 + u * 8 + e]), p.scale_log2, neg_m));
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            pw[u * 4 + q] = pack2<T>(pv[2 * q], pv[2 * q + 1]);
+                            const float2 a = unpack2<T>(pw[u * 4 + q]);
+                            ls[q] += a.x + a.y;
+                        }
+                    }
+                    tmem_st32(tmem + lane_off + kColP + buf * 64 + h * 32, pw);
                 }
+                tmem_wait_st();
                 l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 // key row r past every row's last visible key: its slot may hold anything
                 const bool zero_v = k0 + r >= I.kmax;
