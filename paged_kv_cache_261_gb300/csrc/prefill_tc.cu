@@ -60,7 +60,6 @@ constexpr int kStages = 2;
 constexpr int kChunk = 128 * 128;              // 128 rows x 128 bytes (one 64-element half)
 constexpr int kKVBytes = 2 * kChunk;           // one K (or V) tile
 constexpr int kQBytes = 2 * kChunk;
-constexpr int kPBytes = 2 * kChunk;
 constexpr int kThreads = 224;                  // + warp 6: V producer
 constexpr int kVProdWarp = 6;
 constexpr uint32_t kTmemCols = 512;            // S[2] x 128 + O x 128 + P[2] x 64
@@ -71,8 +70,7 @@ constexpr float kRescaleLog2 = 8.f;            // keep the reference max until a
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kStages * kKVBytes;
 constexpr int kOffQ = kOffV + kStages * kKVBytes;
-constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffBar = kOffP;
+constexpr int kOffBar = kOffQ + kQBytes;
 constexpr int kNumBars = 19;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 16;
