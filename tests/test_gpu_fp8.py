@@ -152,6 +152,26 @@ def test_decode_fp8_ragged_contexts(pa, dtype, bs, H, Hk):
     _errors_clear(pa)
 
 
+@pytest.mark.parametrize("bs,H,Hk,dtype", [(32, 12, 4, "bf16"), (64, 24, 8, "f16"), (32, 6, 2, "f16")])
+def test_decode_fp8_padded_groups_and_block_sizes(pa, bs, H, Hk, dtype):
+    """G = 3 (padded to 4 columns) and block sizes 32 / 64."""
+    w = workloads.make_decode(f"fp8_g{H // Hk}_{bs}", 511 + bs, RAGGED, H, Hk, 128, bs, dtype)
+    out, _, _ = gpu_decode_fp8(w, max_context_len=int(RAGGED.max()))
+    assert_close(to_f64(out), oracle_decode_fp8(w, range(w.num_seqs)), dtype, f"fp8 bs{bs} H{H}/{Hk} {dtype}")
+    _errors_clear(pa)
+
+
+def test_decode_fp8_many_partitions_split_the_launch(pa):
+    rng = np.random.default_rng(512)
+    ctx = rng.integers(19000, 20000, size=64).astype(np.int32)
+    ctx[[5, 40]] = [1, 20000]
+    w = workloads.make_decode("fp8_many_items", 512, ctx, 32, 8, 128, 16, "bf16")
+    out, _, _ = gpu_decode_fp8(w, max_context_len=20000, partition_size=128)
+    seqs = [0, 5, 30, 31, 32, 40, 63]
+    assert_close(to_f64(out)[seqs], oracle_decode_fp8(w, seqs), "bf16", "fp8 split launch")
+    _errors_clear(pa)
+
+
 @pytest.mark.parametrize("partition_size", [128, 256, 1024])
 def test_decode_fp8_partition_sizes(pa, partition_size):
     w = workloads.make_decode("fp8_parts", 509, RAGGED, 32, 8, 128, 16, "bf16")

@@ -421,3 +421,17 @@ def test_large_batch_runs_in_chunks(pa):
     ref = oracle_decode(w, seqs)
     assert_close(to_f64(out)[seqs], ref, "bf16", "2500 sequences")
     _errors_clear(pa)
+
+
+def test_many_partitions_split_the_launch(pa):
+    """64 sequences x 8 kv heads x 157 partitions of 128 tokens is more work items
+    than one persistent grid's per-CTA tables hold: the library splits the batch
+    into independent launches; every row must still match the oracle."""
+    rng = np.random.default_rng(43)
+    ctx = rng.integers(19000, 20000, size=64).astype(np.int32)
+    ctx[[0, 17, 63]] = [20000, 1, 12345]
+    w = workloads.make_decode("many_items", 43, ctx, 32, 8, 128, 16, "bf16")
+    out, kc, vc = gpu_decode(w, max_context_len=20000, partition_size=128)
+    seqs = [0, 1, 17, 30, 31, 32, 60, 61, 62, 63]
+    assert_close(to_f64(out)[seqs], oracle_decode(w, seqs), "bf16", "split launch")
+    _errors_clear(pa)

@@ -64,6 +64,7 @@ def oracle_prefill(pw):
     (8, 8, 32, "f16"),       # G = 1
     (12, 4, 8, "bf16"),      # G = 3, padded to 4
     (32, 2, 128, "f16"),     # G = 16
+    (16, 4, 64, "bf16"),     # G = 4, block size 64
 ])
 def test_chunked_prefill_against_oracle(pa, H, Hk, bs, dtype):
     prior = np.array([0, 5, 130, 700, 31, 0, 1000], np.int32)

@@ -125,6 +125,14 @@ def test_prefix_lengths_off_block_boundaries(pa, cut):
     assert_close(to_f64(out), _oracle_full(w, np.arange(w.num_seqs)), "bf16", f"prefix cut {cut}")
 
 
+def test_random_groups_f16(pa):
+    groups = [(4, 6, 60), (6, 20, 200), (2, 3, 0)]
+    w = workloads.make_shared_groups(71, groups, 4, 32, 8, 128, 16, "f16")
+    plain, shared, pl, gm = _run(pa, w, 8)
+    assert pa.get_device_error() == 0
+    assert_close(to_f64(shared), _oracle_full(w, np.arange(w.num_seqs)), "f16", "groups f16")
+
+
 def test_no_groups_equals_plain_decode(pa):
     w = workloads.llama8b_decode(num_seqs=12)
     plain, shared, pl, gm = _run(pa, w, 8)
