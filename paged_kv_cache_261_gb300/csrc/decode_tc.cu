@@ -487,9 +487,9 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                     uint4 *v0 = reinterpret_cast<uint4 *>(sV + stage * kKVBytes + row * 128);
                     uint4 *v1 = reinterpret_cast<uint4 *>(sV + stage * kKVBytes + kChunkBytes + row * 128);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        v0[c] = make_uint4(0, 0, 0, 0);
-                        v1[c] = make_uint4(0, 0, 0, 0);
+                    for (int c = 0; c < 8; ++c) {           // rotated by row: no bank conflicts
+                        v0[c ^ (row & 7)] = make_uint4(0, 0, 0, 0);
+                        v1[c ^ (row & 7)] = make_uint4(0, 0, 0, 0);
                     }
                 }
                 fence_proxy_async_smem();

@@ -542,9 +542,9 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                     uint4 *v0 = reinterpret_cast<uint4 *>(sV + buf * kKVBytes + r * 128);
                     uint4 *v1 = reinterpret_cast<uint4 *>(sV + buf * kKVBytes + kChunk + r * 128);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        v0[c] = make_uint4(0, 0, 0, 0);
-                        v1[c] = make_uint4(0, 0, 0, 0);
+                    for (int c = 0; c < 8; ++c) {           // rotated by row: no bank conflicts
+                        v0[c ^ (r & 7)] = make_uint4(0, 0, 0, 0);
+                        v1[c ^ (r & 7)] = make_uint4(0, 0, 0, 0);
                     }
                 }
                 fence_proxy_async_smem();
