@@ -294,14 +294,18 @@ int pa_paged_kv_write_fp8(const void *k, const void *v, const int32_t *slot_mapp
  *   out[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . k_scale*K8[b,t,h/G,:])
  *                * v_scale*V8[b,t,h/G,:]
  *
- * q and out have dtype PA_DTYPE_BF16 or PA_DTYPE_F16. Codes are expanded to
- * that type exactly; accumulation is fp32. Supported: head_dim 128,
- * num_heads / num_kv_heads <= 16, block_size a power of two in [8, 128];
- * PA_ERR_UNSUPPORTED otherwise. Partitions, max_context_len, the workspace
- * (size from pa_decode_workspace_bytes; NULL = cudaMallocAsync on the stream)
- * and the device error bits are those of pa_paged_attention_decode. The caches
- * must hold finite codes: a NaN code is read as NaN on the f16 path and as
- * 480 on the bf16 path (the write never stores a NaN code from a finite input).
+ * q and out have dtype PA_DTYPE_BF16 or PA_DTYPE_F16. The codes are the
+ * tensor-core operands as stored (E4M3 x E4M3 products, fp32 accumulation);
+ * the query and the softmax weights enter those products as sums of two E4M3
+ * terms: a query row scaled by a power of two is exact for bf16 (8 of an
+ * f16's 11 significant bits), and a weight keeps about a bf16's precision.
+ * Supported: head_dim 128, num_heads / num_kv_heads <= 16, block_size a power
+ * of two in [8, 128]; PA_ERR_UNSUPPORTED otherwise. Partitions,
+ * max_context_len, the workspace (size from pa_decode_workspace_bytes; NULL =
+ * cudaMallocAsync on the stream) and the device error bits are those of
+ * pa_paged_attention_decode. A NaN code inside a context makes the outputs of
+ * its heads NaN (the write never stores one from a finite input); codes in
+ * the slots past a context's end are never used, whatever they hold.
  */
 int pa_paged_attention_decode_fp8(void *out, const void *q, const void *key_cache,
                                   const void *value_cache, const int32_t *block_tables,

@@ -634,6 +634,7 @@ int launch_decode_tc(const DecodeParams &p, int dtype, cudaStream_t stream) {
         c.out = static_cast<char *>(p.out) + rows * kD * 2;
         c.block_tables = p.block_tables + (int64_t)b0 * p.max_blocks_per_seq;
         c.context_lens = p.context_lens + b0;
+        if (p.prefix_lens) c.prefix_lens = p.prefix_lens + b0;
         if (p.ws_ml) {
             c.ws_ml = p.ws_ml + rows * p.max_partitions * 2;
             c.ws_o = p.ws_o + rows * p.max_partitions * kD;

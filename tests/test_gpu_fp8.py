@@ -1,9 +1,11 @@
 """GPU parity of the 8-bit (OCP FP8 E4M3) cache path against the CPU oracle.
 
 Scatter and block copy: bit-exact codes. Decode: max/mean abs error within
-2e-2 / 2e-3 for bf16 and fp16 outputs -- the codes expand exactly into the
-16-bit operand type, so the error budget is that of the 16-bit decode (P in
-16 bits, fp32 accumulation, the output rounded once).
+2e-2 / 2e-3 for bf16 and fp16 outputs. The kernel multiplies the codes as
+stored; the query enters as two E4M3 terms (exact for bf16, 8 significant
+bits for f16) and each softmax weight as two E4M3 terms (about a bf16's
+precision), so the error budget is that of the 16-bit decode (P in 16 bits,
+fp32 accumulation, the output rounded once).
 """
 import numpy as np
 import pytest

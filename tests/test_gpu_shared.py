@@ -125,6 +125,20 @@ def test_prefix_lengths_off_block_boundaries(pa, cut):
     assert_close(to_f64(out), _oracle_full(w, np.arange(w.num_seqs)), "bf16", f"prefix cut {cut}")
 
 
+def test_batch_above_one_launch_reads_its_own_prefix_lengths(pa):
+    """More sequences than one partition launch takes (512): the launch for
+    sequences 512.. must read their own shared-prefix lengths. Prefix lengths
+    cycle through 2..8 blocks, so another launch's lengths would be wrong."""
+    groups = [(10, 2 + (i % 7), 40) for i in range(60)]
+    w = workloads.make_shared_groups(83, groups, 20, 32, 8, 128, 16, "bf16")
+    assert w.num_seqs > 512
+    plain, shared, pl, gm = _run(pa, w, 10)
+    assert pa.get_device_error() == 0
+    assert np.abs(to_f64(plain) - to_f64(shared)).max() <= 2e-2
+    seqs = np.arange(500, w.num_seqs, 5)
+    assert_close(to_f64(shared)[seqs], _oracle_full(w, seqs), "bf16", "shared decode, second launch")
+
+
 def test_random_groups_f16(pa):
     groups = [(4, 6, 60), (6, 20, 200), (2, 3, 0)]
     w = workloads.make_shared_groups(71, groups, 4, 32, 8, 128, 16, "f16")
