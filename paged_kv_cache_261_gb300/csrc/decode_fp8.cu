@@ -29,14 +29,17 @@
 // zeros before the P.V product, since a stale code may be NaN and 0 x NaN is
 // NaN.
 //
-// CTA = one persistent worker per SM; 320 threads:
+// CTA = a persistent worker, two per SM (one for groups above 8, whose softmax
+// needs more registers): each tile's chain of S product, softmax barriers and
+// P.V product is latency-bound, and a second independent chain on the SM hides
+// much of it. 320 threads:
 //   warp 0     TMA producer of the K boxes (128 codes x block_size tokens of one
 //              kv head per physical block, 128-byte rows, 128-byte swizzle) into
-//              a 4-stage ring.
-//   warp 7     TMA producer of the V boxes into a 6-stage ring (a V stage is held
+//              a 2-stage ring.
+//   warp 7     TMA producer of the V boxes into a 3-stage ring (a V stage is held
 //              until the P.V product, after the softmax).
 //   warp 8     query split: per item, the group's query rows -> hi/lo code rows
-//              and per-head score scales, into a 4-slot ring.
+//              and per-head score scales, into a 2-slot ring.
 //   warp 9     L2 prefetch of the blocks up to two tiles ahead of the K loads.
 //   warp 1     S MMA issuer (one thread) and tensor-memory owner.
 //   warp 6     P.V MMA issuer (one thread).
@@ -62,9 +65,9 @@ using decode_order::Item;
 constexpr int kD = 128;
 constexpr int kTile = 128;                        // tokens per MMA tile (M of the S product)
 constexpr int kMaxG = 16;                         // query heads per kv head
-constexpr int kKStages = 4;
-constexpr int kVStages = 6;
-constexpr int kQSlots = 4;
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
+constexpr int kQSlots = 2;
 constexpr int kTileBytes = kTile * kD;            // 128 rows x 128 codes
 constexpr int kOpBytes = 32 * 128;                // one hi/lo operand: up to 32 rows x 128 codes
 constexpr int kThreads = 320;
@@ -73,6 +76,8 @@ constexpr int kPrefetchTiles = 2;                 // L2 prefetch distance, in ti
 constexpr int kMaxSeqs = 512;                     // sequences per launch (the host splits larger batches)
 constexpr uint32_t kTmemCols = 128;               // S[2] and O[2], N columns each
 
+// Resident CTAs per SM: two (96 registers a thread) where the softmax fits them.
+__host__ __device__ constexpr int ctas_per_sm(int gt) { return gt <= 8 ? 2 : 1; }
 // MMA N: hi and lo rows of GT heads, at least 16.
 __host__ __device__ constexpr int n_cols(int gt) { return 2 * gt < 16 ? 16 : 2 * gt; }
 
@@ -108,7 +113,7 @@ constexpr int kOffPs = kOffCtx + kMaxSeqs * 4;                // int [kMaxSeqs] 
 constexpr int kSmemUsed = kOffPs + kMaxSeqs * 4;
 static_assert(kSmemUsed - kOffPrefix >= decode_order::kTableItems * 16, "item table fits the ordering arrays");
 constexpr int kSmemBytes = kSmemUsed + 1024;                  // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kSmemBytes <= 115712, "shared memory budget: two CTAs per SM");
 static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOpBytes % 1024 == 0,
               "128-byte-swizzled tiles need 1024-byte alignment");
 static_assert(2 * kOpBytes >= kMaxSeqs, "the P rows serve as the ordering scratch");
@@ -211,7 +216,7 @@ template <> __device__ __forceinline__ void unpack4<__half>(uint2 u, float *x) {
 }
 
 template <typename T, int GT>
-__global__ __launch_bounds__(kThreads, 1) void decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k,
+__global__ __launch_bounds__(kThreads, ctas_per_sm(GT)) void decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
                                                                  const DecodeParams p, const float v_scale) {
     constexpr int NT = n_cols(GT);
@@ -747,7 +752,8 @@ int launch_t(const DecodeParams &p, float v_scale, cudaStream_t stream) {
     CUtensorMap mk, mv;
     if (!make_cache_map_u8(&mk, p.key_cache, p) || !make_cache_map_u8(&mv, p.value_cache, p)) return -1;
     const int64_t max_items = (int64_t)p.num_seqs * p.num_kv_heads * p.max_partitions;
-    const int grid = (int)(max_items < num_sms[dev] ? max_items : num_sms[dev]);
+    const int64_t slots = (int64_t)ctas_per_sm(GT) * num_sms[dev];
+    const int grid = (int)(max_items < slots ? max_items : slots);
     return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, stream, mk, mv, p, v_scale);
 }
 
@@ -776,7 +782,8 @@ int launch_decode_fp8(const DecodeParams &p, float v_scale, int dtype, cudaStrea
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return -1;
     const int64_t per_seq = (int64_t)p.num_kv_heads * p.max_partitions;
-    const int64_t by_items = (int64_t)decode_order::kTableItems * sms / (per_seq > 0 ? per_seq : 1);
+    const int cps = p.group <= 8 ? ctas_per_sm(8) : ctas_per_sm(16);
+    const int64_t by_items = (int64_t)decode_order::kTableItems * cps * sms / (per_seq > 0 ? per_seq : 1);
     const int chunk = (int)(by_items < 1 ? 1 : (by_items < kMaxSeqs ? by_items : kMaxSeqs));
     for (int b0 = 0; b0 < p.num_seqs; b0 += chunk) {
         DecodeParams c = p;
