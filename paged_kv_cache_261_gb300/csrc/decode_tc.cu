@@ -115,10 +115,11 @@ struct Bars {
 using decode_order::Item;
 using decode_order::get_item;
 
+// Largest value over the warp in one instruction (exact, as any max).
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
