@@ -40,7 +40,9 @@
 //              until the P.V product, after the softmax).
 //   warp 8     query split: per item, the group's query rows -> hi/lo code rows
 //              and per-head score scales, into a 2-slot ring.
-//   warp 9     L2 prefetch of the blocks up to two tiles ahead of the K loads.
+//   warp 9     L2 prefetch of the next tile's blocks, ahead of the K loads (groups
+//              up to 4; with larger groups the softmax, not the loads, sets the pace,
+//              and the extra L2 traffic only costs).
 //   warp 1     S MMA issuer (one thread) and tensor-memory owner.
 //   warp 6     P.V MMA issuer (one thread).
 //   warps 2-5  softmax and output (thread = token for S, = dim for O).
@@ -72,7 +74,7 @@ constexpr int kTileBytes = kTile * kD;            // 128 rows x 128 codes
 constexpr int kOpBytes = 32 * 128;                // one hi/lo operand: up to 32 rows x 128 codes
 constexpr int kThreads = 320;
 constexpr int kPvWarp = 6, kVProdWarp = 7, kQWarp = 8, kPrefetchWarp = 9;
-constexpr int kPrefetchTiles = 2;                 // L2 prefetch distance, in tiles, ahead of the K loads
+constexpr int kPrefetchTiles = 1;                 // L2 prefetch distance, in tiles, ahead of the K loads
 constexpr int kMaxSeqs = 512;                     // sequences per launch (the host splits larger batches)
 constexpr uint32_t kTmemCols = 128;               // S[2] and O[2], N columns each
 
@@ -508,7 +510,7 @@ __global__ __launch_bounds__(kThreads, ctas_per_sm(GT)) void decode_fp8_kernel(c
         // hints: if this warp falls behind or gives up, only speed changes.
         const int nbt = kTile / p.block_size;
         uint32_t n = 0;
-        bool go = true;
+        bool go = GT <= 4;
         for (int k = 0; k < nmy && go; ++k) {
             const Item I = decode_order::unpack_item(items[k]);
             const decode_order::ItemTable tb = decode_order::load_item_table(p, I, lane);
