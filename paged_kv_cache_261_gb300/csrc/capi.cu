@@ -253,7 +253,8 @@ int pa_paged_kv_write_fp8(const void *k, const void *v, const int32_t *slot_mapp
     if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache))
         return PA_ERR_INVALID_ARG;
     if (num_blocks > INT64_MAX / block_size) return PA_ERR_INVALID_ARG;
-    if ((num_tokens + 7) / 8 > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    const int64_t runs = 2 * (row_elems / 16);          // one thread per 16-element run of K or V
+    if (num_tokens > INT64_MAX / runs || (num_tokens * runs + 255) / 256 > INT32_MAX) return PA_ERR_UNSUPPORTED;
     unsigned int *err = nullptr;
     if (int rc = error_word(&err)) return rc;
     if (pa::launch_kv_write_fp8(k, v, src_dtype, slot_mapping, num_tokens, key_cache, value_cache,

@@ -6,15 +6,16 @@
 // head_dim] cache). The 8-bit encoding is not on the pages: each element x is
 // stored as the E4M3 code nearest to x / scale, the quotient taken in float32
 // with IEEE division and rounded to the code by the hardware conversion
-// (round to nearest even, saturating to +-448). One warp per token; a lane
-// turns 16 source elements into one 16-byte run of codes.
+// (round to nearest even, saturating to +-448). One thread per 16-element run
+// of one token's K or V row: it turns 16 source elements into one 16-byte run
+// of codes, so even a batch of a few tokens spreads its divisions over the GPU.
 #include "common.cuh"
 #include "kernels_fp8.h"
 
 namespace pa {
 namespace {
 
-constexpr int kWarps = 8;       // tokens per CTA
+constexpr int kThreads = 256;
 
 // 16 consecutive source elements (16-byte aligned) as floats.
 template <typename TS>
@@ -44,42 +45,39 @@ __device__ __forceinline__ uint4 encode16(const float *x, float scale) {
 }
 
 template <typename TS>
-__global__ __launch_bounds__(kWarps * 32) void kv_write_fp8_kernel(
+__global__ __launch_bounds__(kThreads) void kv_write_fp8_kernel(
     const TS *__restrict__ k, const TS *__restrict__ v, const int32_t *__restrict__ slots, int64_t num_tokens,
     uint4 *__restrict__ kc, uint4 *__restrict__ vc, int64_t num_slots, int row_elems, float k_scale,
     float v_scale, unsigned int *err) {
     // a decode launched after this kernel may start its set-up now; it waits for
     // this grid to finish before reading the cache
     asm volatile("griddepcontrol.launch_dependents;");
-    const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int groups = row_elems / 16;              // 16-element runs per row
+    const int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t t = idx / (2 * groups);           // token; then K runs, then V runs
     if (t >= num_tokens) return;
+    const int r = (int)(idx - t * 2 * groups);
     const int64_t slot = slots[t];
     if (slot == -1) return;
     if (slot < 0 || slot >= num_slots) {
-        if (lane == 0) raise_error(err, PA_DEVERR_SLOT);
+        if (r == 0) raise_error(err, PA_DEVERR_SLOT);
         return;
     }
-    const int groups = row_elems / 16;
-    const TS *ks = k + t * row_elems;
-    const TS *vs = v + t * row_elems;
-    uint4 *kd = kc + slot * groups;
-    uint4 *vd = vc + slot * groups;
-    for (int g = lane; g < groups; g += 32) {
-        float xk[16], xv[16];
-        load16(ks + g * 16, xk);
-        load16(vs + g * 16, xv);
-        kd[g] = encode16(xk, k_scale);
-        vd[g] = encode16(xv, v_scale);
-    }
+    const bool is_v = r >= groups;
+    const int g = is_v ? r - groups : r;
+    float x[16];
+    load16((is_v ? v : k) + t * row_elems + g * 16, x);
+    (is_v ? vc : kc)[slot * groups + g] = encode16(x, is_v ? v_scale : k_scale);
 }
 
 template <typename TS>
 int launch_t(const void *k, const void *v, const int32_t *slots, int64_t num_tokens, void *kc, void *vc,
              int64_t num_slots, int row_elems, float k_scale, float v_scale, unsigned int *err,
              cudaStream_t stream) {
-    const int64_t grid = (num_tokens + kWarps - 1) / kWarps;
-    kv_write_fp8_kernel<TS><<<(unsigned)grid, kWarps * 32, 0, stream>>>(
+    const int64_t threads = num_tokens * 2 * (row_elems / 16);
+    const int64_t grid = (threads + kThreads - 1) / kThreads;
+    if (grid > 0x7FFFFFFF) return -2;
+    kv_write_fp8_kernel<TS><<<(unsigned)grid, kThreads, 0, stream>>>(
         static_cast<const TS *>(k), static_cast<const TS *>(v), slots, num_tokens, static_cast<uint4 *>(kc),
         static_cast<uint4 *>(vc), num_slots, row_elems, k_scale, v_scale, err);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;

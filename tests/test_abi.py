@@ -140,6 +140,7 @@ def test_write_fp8_rejects_bad_arguments(pa):
     assert w(hk=1, d=8) == -2            # rows of 8 codes: not a multiple of 16
     assert w(T=0) == 0                   # nothing to do
     assert w(k=8) == -1                  # misaligned
+    assert w(T=2 ** 40) == -2            # one thread per 16-element run: beyond one launch
     # copy_blocks takes the 8-bit storage code
     assert L.pa_copy_blocks(16, 16, 16, 0, 8, 16, 8, 128, 3, None) == 0
 
