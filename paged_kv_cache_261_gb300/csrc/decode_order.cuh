@@ -145,7 +145,11 @@ __device__ __forceinline__ void build(const DecodeParams &p, int *prefix, int *o
 }
 
 // ---- per-CTA item table ----------------------------------------------------------
-// A CTA works on items blockIdx.x, blockIdx.x + gridDim.x, ...; its k-th item's
+// Items are dealt in rounds of gridDim.x, serpentine: in even rounds CTA b takes
+// the round's b-th item, in odd rounds its (gridDim.x - 1 - b)-th. Down a list
+// sorted by decreasing size this evens the CTAs' totals (a CTA that took a larger
+// item in one round takes a smaller one in the next); round-robin left the 8B-shaped
+// batch's most loaded CTA 62 tiles against a mean of 59.9. A CTA's k-th item's
 // descriptor is computed once, in parallel, and kept in shared memory (16 bytes),
 // so no role repeats the search and the divisions of get_item at every item.
 constexpr int kTableItems = 512;       // items per CTA the table holds (8 KiB)
@@ -165,12 +169,20 @@ __device__ __forceinline__ Item unpack_item(int4 d) {
     it.ntiles = it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
     return it;
 }
-// Items of this CTA. The host sizes launches so that this never exceeds
-// kTableItems; the clamp only keeps every table access inside the table.
+// Index of this CTA's k-th item.
+__device__ __forceinline__ int cta_item_index(int k) {
+    const int g = (int)gridDim.x, b = (int)blockIdx.x;
+    return k * g + ((k & 1) ? g - 1 - b : b);
+}
+// Items of this CTA: one per full round, plus one in the last, partial round if
+// its position there falls below the remainder. The host sizes launches so that
+// this never exceeds kTableItems; the clamp only keeps every table access inside
+// the table.
 __device__ __forceinline__ int cta_items(int total_items) {
-    const int n = total_items > (int)blockIdx.x
-                      ? (total_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
-                      : 0;
+    const int g = (int)gridDim.x, b = (int)blockIdx.x;
+    const int rounds = total_items / g, rem = total_items - rounds * g;
+    const int pos = (rounds & 1) ? g - 1 - b : b;
+    const int n = rounds + (pos < rem ? 1 : 0);
     return n < kTableItems ? n : kTableItems;
 }
 // Every thread of the CTA calls this after build() and a barrier. The table is
@@ -184,7 +196,7 @@ __device__ __forceinline__ void build_item_table(const DecodeParams &p, const in
 #pragma unroll
     for (int u = 0; u < kPerThread; ++u) {
         const int k = (int)threadIdx.x + u * (int)blockDim.x;
-        if (k < n) d[u] = pack_item(get_item((int)blockIdx.x + k * (int)gridDim.x, prefix, order, n4, p, c));
+        if (k < n) d[u] = pack_item(get_item(cta_item_index(k), prefix, order, n4, p, c));
     }
     __syncthreads();
 #pragma unroll
