@@ -351,19 +351,27 @@ __device__ __forceinline__ void merge_row(const DecodeParams &p, int b, int h, i
 constexpr int kWarpRowMaxParts = 32;
 
 template <typename T, int VEC>
-__device__ __forceinline__ void merge_row_warp(const DecodeParams &p, int b, int h, int nparts) {
+__device__ __forceinline__ void merge_row_warp(const DecodeParams &p, int b, int h) {
     const int lane = threadIdx.x & 31;
     const int D = p.head_dim, P = p.max_partitions;
     const int64_t row0 = ((int64_t)b * p.num_heads + h) * P;
+    // The (m, l) pairs are read together with the sequence's length (one round
+    // trip, not two); entries past its partition count lie inside its row of the
+    // workspace and are ignored. The partials themselves are read once the count
+    // is known: rows written directly by the partition kernel read none.
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + row0;
-    const float2 mine = lane < nparts ? ml[lane] : make_float2(-INFINITY, 0.f);
+    float2 mine = lane < P ? ml[lane] : make_float2(-INFINITY, 0.f);
+    const SeqSplit sp = seq_split(p, b);
+    if (sp.direct) return;                      // the partition kernel wrote the row
+    const int nparts = sp.shared + sp.priv;
+    if (lane >= nparts) mine = make_float2(-INFINITY, 0.f);
     float M = mine.x;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float e = lane < nparts ? fast_exp2(mine.x - M) : 0.f;
     float L = mine.y * e;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     const float c_mine = e / L;
     float acc[VEC];
 #pragma unroll
@@ -395,11 +403,8 @@ __global__ __launch_bounds__(kReduceThreads) void decode_reduce_warp_kernel(cons
     const int64_t row = (int64_t)blockIdx.x * kReduceWarps + (threadIdx.x >> 5);
     if (row >= (int64_t)p.num_seqs * p.num_heads) return;
     const int b = (int)(row / p.num_heads), h = (int)(row % p.num_heads);
-    const SeqSplit sp = seq_split(p, b);
-    if (sp.direct) return;                      // the partition kernel wrote the row
-    const int nparts = sp.shared + sp.priv;
-    if (p.head_dim == 128) merge_row_warp<T, 4>(p, b, h, nparts);
-    else merge_row_warp<T, 2>(p, b, h, nparts);
+    if (p.head_dim == 128) merge_row_warp<T, 4>(p, b, h);
+    else merge_row_warp<T, 2>(p, b, h);
 }
 
 template <typename T>
