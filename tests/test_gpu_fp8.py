@@ -221,6 +221,37 @@ def test_decode_fp8_large_batch_runs_in_chunks(pa):
     _errors_clear(pa)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_decode_fp8_query_magnitudes_per_head(pa, dtype):
+    """The query enters the 8-bit MMAs as two E4M3 terms after a power-of-two scale
+    chosen per head. Heads of one group get magnitudes 2^-130 (bf16 subnormals; f16
+    flushes them to zero), 2^-12, 2^4 and exactly 0 (a uniform softmax): each head's
+    scale is its own, and the clamped and all-zero cases still match the oracle."""
+    w = workloads.make_decode("fp8_qmag", 508, np.array([1, 100, 700, 1500], np.int32), 16, 4, 128, 16, dtype)
+    d = dev()
+    dt = workloads.torch_dtype(dtype)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    kc = torch.full(shape, FP8_POISON, dtype=torch.uint8, device=d)
+    vc = torch.full(shape, FP8_POISON, dtype=torch.uint8, device=d)
+    w.fill_cache_torch(kc, vc, include_newest=True)
+    factor = torch.tensor([2.0 ** -130, 2.0 ** -12, 2.0 ** 4, 0.0], dtype=torch.float64)
+    factor = factor.repeat(w.num_heads // 4)[None, :, None]
+    q64 = w.q_values(like=kc).double().cpu() * factor
+    q = q64.to(dt).to(d).contiguous()
+    out = torch.full_like(q, float("nan"))
+    pa.paged_attention_decode_fp8(out, q, kc, vc, torch.as_tensor(w.block_tables, device=d),
+                                  torch.as_tensor(w.context_lens, device=d), w.scale, S, S)
+    torch.cuda.synchronize()
+    assert pa.get_device_error() == 0
+    seqs = np.arange(w.num_seqs)
+    view = w.compact_host_view(seqs, include_newest=True, codes=True)
+    qh = workloads.to_storage_numpy(q.float().cpu().numpy(), dtype)
+    ref = oracle.paged_attention_fp8(qh, view["key_cache"], view["value_cache"], view["block_tables"],
+                                     view["context_lens"], w.scale, S, S, dtype,
+                                     num_threads=oracle.num_host_threads())
+    assert_close(to_f64(out), ref, dtype, f"fp8 query magnitudes {dtype}")
+
+
 def test_decode_fp8_single_token_is_dequantised_v(pa):
     """ctx = 1: the softmax weight is 1, so out = v_scale * decoded(V code) rounded once."""
     w = workloads.make_decode("fp8_one", 505, np.array([1, 1, 1], np.int32), 16, 4, 128, 8, "bf16")
