@@ -55,6 +55,7 @@ struct PrefillParams {
     int group_pad;              // group rounded up to a power of two
     int rows_q;                 // query tokens per item: 128 / group_pad
     int qtiles;                 // ceil(max_query_len / rows_q)
+    int sorted_items;           // set by the launcher: deal items largest first (see prefill_tc.cu)
     int head_dim;
     int block_size;
     int log2_block_size;

@@ -35,8 +35,14 @@
 //   warp 1     one thread issues the MMAs and owns tensor memory.
 //   warps 2-5  softmax (scale, causal mask, exp2, P to tensor memory, V rows of
 //              keys past the last visible one zeroed) and the epilogue O / l.
-// Items are ordered with the query tiles of one (sequence, kv head) adjacent,
-// so the CTAs working on them at the same time share its K/V through L2.
+// Items differ in size by up to the context length (key tiles = causal extent
+// / 128), and a persistent CTA ends with its last item: dealt in index order the
+// most loaded CTA of the chunked-prefill batch had 13 % more key tiles than the
+// mean. So each CTA first sorts the (sequence, query tile) entries by key-tile
+// count, largest first (a counting sort, stable by index, so every CTA derives
+// the same order), and takes every grid-th item of that list in serpentine
+// rounds; an entry's kv heads stay adjacent. Batches too large for the sort's
+// scratch (which lives in the K/V rings before the first load) keep index order.
 // Every wait is bounded; on a timeout the kernel sets PA_DEVERR_WAIT and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -73,7 +79,17 @@ constexpr int kOffQ = kOffV + kStages * kKVBytes;
 constexpr int kOffBar = kOffQ + kQBytes;
 constexpr int kNumBars = 19;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemUsed = kOffMisc + 16;
+constexpr int kSortBuckets = 1024;             // key-tile counts; larger ones share the last bucket
+constexpr int kSortMaxEntries = 16384;         // (sequence, query tile) entries the sort takes
+constexpr int kMaxMyItems = 1024;              // a CTA's items after the sort
+constexpr int kOffMy = kOffMisc + 16;          // int [kMaxMyItems]: this CTA's items, in order
+constexpr int kSmemUsed = kOffMy + kMaxMyItems * 4;
+// sort scratch, in the K/V rings (unused until the first load)
+constexpr int kOffSortSize = kOffK;                                  // uint16 [kSortMaxEntries]
+constexpr int kOffSorted = kOffSortSize + 2 * kSortMaxEntries;       // uint16 [kSortMaxEntries]
+constexpr int kOffCursor = kOffSorted + 2 * kSortMaxEntries;         // int [kSortBuckets]
+static_assert(kOffCursor + 4 * kSortBuckets <= kOffQ, "sort scratch fits the rings");
+static_assert(kSortMaxEntries <= 65536, "entries fit 16 bits");
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -134,6 +150,97 @@ __device__ __forceinline__ bool get_gitem(int idx, const PrefillParams &p, PItem
     it.q_row0 = 0;
     it.nq = n;
     return true;
+}
+
+// Key tiles of (sequence, query tile) entry e = b * qtiles + qt, as get_pitem
+// would give them; 0 for an empty tile or an inconsistent sequence (reported here,
+// by CTA 0: such entries never reach the roles).
+__device__ __forceinline__ int entry_tiles(const PrefillParams &p, int e) {
+    const int b = e / p.qtiles, qt = e - b * p.qtiles;
+    const int q_start = p.query_start_loc[b];
+    const int q_len = p.query_start_loc[b + 1] - q_start;
+    const int ctx = p.context_lens[b];
+    if (q_len < 0 || q_len > p.max_query_len || ctx < q_len || ctx > p.context_limit || q_start < 0 ||
+        (int64_t)q_start + q_len > p.num_query_tokens) {
+        if (qt == 0 && blockIdx.x == 0) raise_error(p.err, PA_DEVERR_CONTEXT);
+        return 0;
+    }
+    const int qi0 = qt * p.rows_q;
+    if (qi0 >= q_len) return 0;
+    const int kmax = ctx - q_len + qi0 + min(p.rows_q, q_len - qi0);
+    const int t = (kmax + kKT - 1) / kKT;
+    return t < kSortBuckets - 1 ? t : kSortBuckets - 1;
+}
+
+// This CTA's items, largest first across the grid (see the header). Every thread
+// calls this; the caller synchronises before the rings are loaded.
+__device__ __forceinline__ int sort_my_items(const PrefillParams &p, unsigned char *smem, int *my) {
+    uint16_t *ssz = reinterpret_cast<uint16_t *>(smem + kOffSortSize);
+    uint16_t *sorted = reinterpret_cast<uint16_t *>(smem + kOffSorted);
+    int *cursor = reinterpret_cast<int *>(smem + kOffCursor);
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int E = p.num_seqs * p.qtiles;
+    for (int i = tid; i < kSortBuckets; i += blockDim.x) cursor[i] = 0;
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        const int t = entry_tiles(p, e);
+        ssz[e] = (uint16_t)t;
+        if (t > 0) atomicAdd(&cursor[t], 1);
+    }
+    __syncthreads();
+    if (tid < 32) {
+        // descending exclusive prefix: cursor[t] = entries with more key tiles
+        int cnt[kSortBuckets / 32], tot = 0;
+#pragma unroll
+        for (int i = 0; i < kSortBuckets / 32; ++i) {
+            cnt[i] = cursor[kSortBuckets - 1 - (lane * (kSortBuckets / 32) + i)];
+            tot += cnt[i];
+        }
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - tot;
+#pragma unroll
+        for (int i = 0; i < kSortBuckets / 32; ++i) {
+            cursor[kSortBuckets - 1 - (lane * (kSortBuckets / 32) + i)] = run;
+            run += cnt[i];
+        }
+        __syncwarp();
+        // stable placement, 32 entries at a time in index order
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int t = e < E ? ssz[e] : 0;
+            const unsigned m = __match_any_sync(0xffffffffu, t);
+            const int leader = __ffs(m) - 1;
+            int pos = 0;
+            if (lane == leader && t > 0) pos = cursor[t];
+            pos = __shfl_sync(0xffffffffu, pos, leader);
+            if (t > 0) sorted[pos + __popc(m & ((1u << lane) - 1))] = (uint16_t)e;
+            __syncwarp();
+            if (lane == leader && t > 0) cursor[t] = pos + __popc(m);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // entries placed = entries with at least one key tile = the start of bucket 0
+    const int total = cursor[0] * p.num_kv_heads;
+    const int g = (int)gridDim.x, b0 = (int)blockIdx.x;
+    const int rounds = total / g, rem = total - rounds * g;
+    int n = rounds + ((((rounds & 1) ? g - 1 - b0 : b0) < rem) ? 1 : 0);
+    n = n < kMaxMyItems ? n : kMaxMyItems;
+    for (int k = tid; k < n; k += blockDim.x) {
+        const int pk = k * g + ((k & 1) ? g - 1 - b0 : b0);
+        const int q = pk / p.num_kv_heads, kvh = pk - q * p.num_kv_heads;
+        const int e = sorted[q];
+        const int b = e / p.qtiles, qt = e - b * p.qtiles;
+        my[k] = (b * p.num_kv_heads + kvh) * p.qtiles + qt;
+    }
+    fence_proxy_async_smem();            // the rings' next writers are TMA copies
+    __syncthreads();
+    return n;
 }
 
 // Block-table entries of an item's keys, read once at item start with one
@@ -265,6 +372,17 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // the items of this CTA: a sorted list, or every grid-th index
+    int *my_items = reinterpret_cast<int *>(smem + kOffMy);
+    bool use_list = false;
+    int nloop = total_items > (int)blockIdx.x ? (total_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    if constexpr (!kGroup) {
+        if (p.sorted_items) {
+            use_list = true;
+            nloop = sort_my_items(p, smem, my_items);
+        }
+    }
+    auto item_at = [&](int k) { return use_list ? my_items[k] : (int)blockIdx.x + k * (int)gridDim.x; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer: Q and K
@@ -273,7 +391,8 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
         const int nbt = kKT / p.block_size;
         uint32_t it = 0, n = 0;                         // K tiles, items issued
         bool ok = true;
-        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+        for (int k = 0; k < nloop && ok; ++k) {
+            const int idx = item_at(k);
             PItem I;
             if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
             const KeyTable tb = load_key_table(p, I, lane);
@@ -334,7 +453,8 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
         const int nbt = kKT / p.block_size;
         uint32_t it = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+        for (int k = 0; k < nloop && ok; ++k) {
+            const int idx = item_at(k);
             PItem I;
             if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
             const KeyTable tb = load_key_table(p, I, lane);
@@ -389,7 +509,8 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                 mma_commit(&v_empty[j & 1]);
                 return true;
             };
-            for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+            for (int k = 0; k < nloop && ok; ++k) {
+                const int idx = item_at(k);
                 PItem I;
                 if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
                 if (!mbar_wait(q_full, n & 1)) {
@@ -442,7 +563,8 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
         T *out = reinterpret_cast<T *>(p.out);
         uint32_t it = 0, n = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+        for (int k = 0; k < nloop && ok; ++k) {
+            const int idx = item_at(k);
             PItem I;
             if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
             const bool row_valid = qi < I.nq && g < G;
@@ -660,7 +782,10 @@ int launch_prefill_t(const PrefillParams &p, CUtensorMapDataType dt, cudaStream_
                                  : (int64_t)p.num_seqs * p.num_kv_heads * p.qtiles;
     if (items == 0) return 0;
     const int grid = (int)(items < num_sms[dev] ? items : num_sms[dev]);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, mq, p);
+    PrefillParams q = p;
+    const int64_t entries = (int64_t)p.num_seqs * p.qtiles;
+    q.sorted_items = !kGroup && entries <= kSortMaxEntries && (items + grid - 1) / grid <= kMaxMyItems;
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(mk, mv, mq, q);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
