@@ -21,6 +21,8 @@
 // Thread = row for the softmax, so the max and the sum are thread-local; O is
 // rescaled (tcgen05.ld / st of the row) only when a row's max grows by more than
 // 2^8, otherwise the stale reference max is kept (the final O / l is the same).
+// The row sum adds the fp32 weights; the P.V MMA sees them rounded to 16 bits (a
+// relative difference of at most 2^-9 per weight, of either sign).
 //
 // Roles (224 threads, one persistent CTA per SM):
 //   warp 0     TMA: the item's query rows (3-D map over [tokens, heads, dims]),
@@ -305,15 +307,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     } else {
         const __half2 v = __floats2half2_rn(a, b);
         return *reinterpret_cast<const uint32_t *>(&v);
-    }
-}
-template <typename T>
-__device__ __forceinline__ float2 unpack2(uint32_t u) {
-    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
-    } else {
-        const __half2 h = *reinterpret_cast<const __half2 *>(&u);
-        return __half22float2(h);
     }
 }
 
@@ -646,8 +639,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             pw[u * 4 + q] = pack2<T>(pv[2 * q], pv[2 * q + 1]);
-                            const float2 a = unpack2<T>(pw[u * 4 + q]);
-                            ls[q] += a.x + a.y;
+                            ls[q] += pv[2 * q] + pv[2 * q + 1];
                         }
                     }
                     tmem_st32(tmem + lane_off + kColP + buf * 64 + h * 32, pw);
