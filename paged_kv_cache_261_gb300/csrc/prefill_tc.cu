@@ -22,7 +22,8 @@
 // rescaled (tcgen05.ld / st of the row) only when a row's max grows by more than
 // 2^8, otherwise the stale reference max is kept (the final O / l is the same).
 // The row sum adds the fp32 weights; the P.V MMA sees them rounded to 16 bits (a
-// relative difference of at most 2^-9 per weight, of either sign).
+// relative difference of at most 2^-9 per weight, of either sign). The exponent
+// arguments and the sums use the paired fp32 instructions (two lanes each).
 //
 // Roles (224 threads, one persistent CTA per SM):
 //   warp 0     TMA: the item's query rows (3-D map over [tokens, heads, dims]),
@@ -297,6 +298,24 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::
             "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Two fp32 lanes in one instruction (sm_100 and later): a * b + c and a + b.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};"
+        "\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};"
+        "\n\tadd.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
 }
 
 template <typename T>
@@ -626,26 +645,23 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                 }
                 tc_fence_after();
                 const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;    // rows with no visible key: p = 0
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pw[32];                  // keys 64h .. 64h + 63 as 16-bit pairs
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        float pv[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            pv[e] = fast_exp2(fmaf(__uint_as_float(sr[h * 64 + u * 8 + e]), p.scale_log2, neg_m));
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            pw[u * 4 + q] = pack2<T>(pv[2 * q], pv[2 * q + 1]);
-                            ls[q] += pv[2 * q] + pv[2 * q + 1];
-                        }
+                    for (int q = 0; q < 32; ++q) {
+                        const float2 x = ffma2(make_float2(__uint_as_float(sr[h * 64 + 2 * q]),
+                                                           __uint_as_float(sr[h * 64 + 2 * q + 1])), sc2, nm2);
+                        const float2 pv = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        pw[q] = pack2<T>(pv.x, pv.y);
+                        ls2[q & 1] = fadd2(ls2[q & 1], pv);
                     }
                     tmem_st32(tmem + lane_off + kColP + buf * 64 + h * 32, pw);
                 }
                 tmem_wait_st();
-                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
                 // key row r past every row's last visible key: its slot may hold anything
                 const bool zero_v = k0 + r >= I.kmax;
                 if (__any_sync(0xffffffffu, zero_v) && !warp_wait(&v_full[buf], (it >> 1) & 1)) {
