@@ -59,7 +59,7 @@ _KERNEL_SOURCES = {
     "decode_tc": ["decode_tc.cu", "decode_order.cuh", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
     "decode_fp8": ["decode_fp8.cu", "decode_order.cuh", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h",
                    "kernels_fp8.h"],
-    "prefill_tc": ["prefill_tc.cu", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
+    "prefill_tc": ["prefill_tc.cu", "prefill_common.cuh", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
 }
 
 DECODE_WORKLOADS = ("llama8b_decode", "long_context", "mixed_serving")

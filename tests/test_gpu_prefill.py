@@ -79,12 +79,12 @@ def test_chunked_prefill_against_oracle(pa, H, Hk, bs, dtype):
 def test_prefill_beyond_the_sort_keeps_index_order(pa):
     """More (sequence, query tile) entries than the kernel's item sort takes
     (16384): the items are dealt in index order, with the same results. G = 16
-    makes a query tile 8 tokens, so one 1024-token chunk and 129 one-token chunks
-    give 130 x 128 entries."""
-    q_lens = np.array([1024] + [1] * 129, np.int32)
+    makes a query tile 8 tokens, so one 2048-token chunk and 129 one-token chunks
+    give 130 x 256 entries."""
+    q_lens = np.array([2048] + [1] * 129, np.int32)
     prior = (np.arange(130) % 40).astype(np.int32)
     pw = workloads.make_prefill("prefill_many", 77, prior, q_lens, 32, 2, 128, 16, "bf16")
-    assert pw.base.num_seqs * (1024 // 8) > 16384
+    assert pw.base.num_seqs * (2048 // 8) > 16384
     out, _, _ = gpu_prefill(pa, pw)
     assert_close(to_f64(out), oracle_prefill(pw), "bf16", "prefill in index order")
     assert pa.get_device_error() == 0
