@@ -156,6 +156,24 @@ __device__ __forceinline__ float2 e4m3x2_value(uint32_t c) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
+// Two fp32 lanes in one instruction (sm_100 and later): a * b + c and a + b.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};"
+        "\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};"
+        "\n\tadd.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // Byte offset of element (row n, column c) in a 128-byte-swizzled K-major tile of
 // 8-bit elements: 128-byte rows, 16-byte chunks permuted within 8-row groups.
 __device__ __forceinline__ int sw128_byte(int n, int c) { return n * 128 + ((((c >> 4) ^ n) & 7) << 4) + (c & 15); }
@@ -629,8 +647,9 @@ __global__ __launch_bounds__(kThreads, ctas_per_sm(GT)) void decode_fp8_kernel(c
                 float alpha[GT];
                 unsigned char *pb = sP + buf * kOpBytes;
 #pragma unroll
+                const float2 neg1 = make_float2(-1.f, -1.f);
                 for (int g = 0; g < GT; g += 2) {
-                    float x[2];
+                    float mn[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int h = g + e;
@@ -638,14 +657,36 @@ __global__ __launch_bounds__(kThreads, ctas_per_sm(GT)) void decode_fp8_kernel(c
                         const float m_new = fmaxf(m_run[h], tmax);
                         alpha[h] = fast_exp2(m_run[h] - m_new);
                         m_run[h] = m_new;
-                        x[e] = valid ? fast_exp2(sv[h] - m_new) * 256.f : 0.f;
+                        mn[e] = m_new;
                     }
-                    const uint32_t hi = e4m3x2(x[0], x[1]);
-                    const float2 hf = e4m3x2_value(hi);
-                    const uint32_t lo = e4m3x2(x[0] - hf.x, x[1] - hf.y);
-                    const float2 lf = e4m3x2_value(lo);
-                    l_part[g] = fmaf(l_part[g], alpha[g], hf.x + lf.x);
-                    l_part[g + 1] = fmaf(l_part[g + 1], alpha[g + 1], hf.y + lf.y);
+                    // the pair of heads in paired fp32 instructions where the registers
+                    // allow (groups up to 4; at 8 the pairs spilled: 0.281 vs 0.234 ms)
+                    float2 x, hf, lf;
+                    uint32_t hi, lo;
+                    if constexpr (GT <= 4) {
+                        const float2 dl = ffma2(make_float2(mn[0], mn[1]), neg1, make_float2(sv[g], sv[g + 1]));
+                        x = ffma2(make_float2(fast_exp2(dl.x), fast_exp2(dl.y)), make_float2(256.f, 256.f),
+                                  make_float2(0.f, 0.f));
+                        if (!valid) x = make_float2(0.f, 0.f);
+                        hi = e4m3x2(x.x, x.y);
+                        hf = e4m3x2_value(hi);
+                        const float2 res = ffma2(hf, neg1, x);
+                        lo = e4m3x2(res.x, res.y);
+                        lf = e4m3x2_value(lo);
+                        const float2 l2 = ffma2(make_float2(l_part[g], l_part[g + 1]),
+                                                make_float2(alpha[g], alpha[g + 1]), fadd2(hf, lf));
+                        l_part[g] = l2.x;
+                        l_part[g + 1] = l2.y;
+                    } else {
+                        x.x = valid ? fast_exp2(sv[g] - mn[0]) * 256.f : 0.f;
+                        x.y = valid ? fast_exp2(sv[g + 1] - mn[1]) * 256.f : 0.f;
+                        hi = e4m3x2(x.x, x.y);
+                        hf = e4m3x2_value(hi);
+                        lo = e4m3x2(x.x - hf.x, x.y - hf.y);
+                        lf = e4m3x2_value(lo);
+                        l_part[g] = fmaf(l_part[g], alpha[g], hf.x + lf.x);
+                        l_part[g + 1] = fmaf(l_part[g + 1], alpha[g + 1], hf.y + lf.y);
+                    }
                     pb[sw128_byte(g, row)] = (unsigned char)hi;
                     pb[sw128_byte(g + 1, row)] = (unsigned char)(hi >> 8);
                     pb[sw128_byte(GT + g, row)] = (unsigned char)lo;
