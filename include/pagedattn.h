@@ -143,6 +143,35 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
                               size_t workspace_bytes, int dtype, void *stream);
 
 /*
+ * One decode step: pa_paged_kv_write of each sequence's new token, then
+ * pa_paged_attention_decode. [P2 demo 1: a decode step writes the new token's
+ * KV into its slot, then attends over the whole context, that token included;
+ * P3 B.2: slot_mapping]
+ *
+ * k_new, v_new: [num_seqs, num_kv_heads, head_dim] in dtype (16-byte aligned),
+ * the new token of sequence b in row b; slot_mapping[b]: its slot, which must be
+ * the slot of position context_lens[b] - 1 (block_tables[b, (ctx - 1) /
+ * block_size] * block_size + (ctx - 1) % block_size), or -1 for no write (the
+ * only value allowed for an empty context). The other arguments, the result
+ * and the workspace rules are those of pa_paged_attention_decode, and the
+ * caches end as after pa_paged_kv_write.
+ *
+ * Where the tensor-core decode takes the call, it writes each token itself,
+ * before it reads that token's block, instead of a separate scatter launch; a
+ * slot other than that of position ctx - 1 then sets PA_DEVERR_SLOT and is not
+ * written. The block holding a sequence's new token must not be read by another
+ * sequence of the same call (copy-on-write guarantees it). Elsewhere the scatter
+ * runs first, as its own launch.
+ */
+int pa_paged_attention_decode_append(void *out, const void *q, const void *k_new, const void *v_new,
+                                     const int32_t *slot_mapping, void *key_cache, void *value_cache,
+                                     const int32_t *block_tables, int max_blocks_per_seq,
+                                     const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int64_t num_blocks, float scale,
+                                     int max_context_len, int partition_size, void *workspace,
+                                     size_t workspace_bytes, int dtype, void *stream);
+
+/*
  * Decode attention that reads each shared prefix once for all sequences that
  * share it.
  * [P2 demo 3: forked samples share the prompt's blocks by reference count;

@@ -238,6 +238,48 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
     return krc == 0 ? PA_OK : PA_ERR_CUDA;
 }
 
+int pa_paged_attention_decode_append(void *out, const void *q, const void *k_new, const void *v_new,
+                                     const int32_t *slot_mapping, void *key_cache, void *value_cache,
+                                     const int32_t *block_tables, int max_blocks_per_seq,
+                                     const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int64_t num_blocks, float scale,
+                                     int max_context_len, int partition_size, void *workspace,
+                                     size_t workspace_bytes, int dtype, void *stream) {
+    if (elem_size(dtype) == 0) return PA_ERR_INVALID_ARG;
+    pa::DecodeParams p{};
+    int64_t P = 0;
+    int rc = decode_setup(p, P, out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                          num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                          max_context_len, partition_size);
+    if (rc == kNothingToDo) return PA_OK;
+    if (rc != PA_OK) return rc;
+    if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_INVALID_ARG;
+    if ((rc = error_word(&p.err)) != PA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *owned = nullptr;
+    if ((rc = decode_workspace(p, P, workspace, workspace_bytes, s, &owned)) != PA_OK) return rc;
+
+    const DecodeKernel choice = decode_kernel_choice();
+    int krc;
+    if (choice == DecodeKernel::Tc || (choice == DecodeKernel::Auto && pa::decode_tc_supported(p, dtype))) {
+        // the tensor-core kernel writes each sequence's token itself, before reading its block
+        p.app_k = k_new;
+        p.app_v = v_new;
+        p.app_slots = slot_mapping;
+        krc = pa::launch_decode_tc(p, dtype, s);
+    } else {
+        // the scatter, then the decode
+        const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * elem_size(dtype);
+        krc = pa::launch_kv_write(k_new, v_new, slot_mapping, num_seqs, key_cache, value_cache,
+                                  num_blocks * block_size, (int)row_bytes, p.err, s);
+        if (krc == 0) krc = pa::launch_decode_simt(p, dtype, s);
+    }
+    if (krc == 0 && P > 1) krc = pa::launch_decode_reduce(p, dtype, s);
+    if (owned) cudaFreeAsync(owned, s);
+    if (krc == -2) return PA_ERR_UNSUPPORTED;
+    return krc == 0 ? PA_OK : PA_ERR_CUDA;
+}
+
 int pa_paged_kv_write_fp8(const void *k, const void *v, const int32_t *slot_mapping, int64_t num_tokens,
                           void *key_cache, void *value_cache, int64_t num_blocks, int block_size,
                           int num_kv_heads, int head_dim, float k_scale, float v_scale, int src_dtype,

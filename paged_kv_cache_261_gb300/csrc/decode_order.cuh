@@ -21,6 +21,7 @@ constexpr int kTile = 128;   // tokens per tile
 struct Item {
     int b, kvh, part, slot, t0, t1, ntiles;
     bool direct;             // write the final row, not a partial
+    bool last;               // ends at the sequence's context length
 };
 
 // Per-sequence lengths cached in shared memory by build(): the clamped context
@@ -65,6 +66,7 @@ __device__ __forceinline__ Item get_item(int idx, const int *prefix, const int *
     it.direct = sp.direct;
     it.t0 = sp.ps + it.part * p.partition_size;
     it.t1 = min(sp.ctx, it.t0 + p.partition_size);
+    it.last = it.t1 == sp.ctx;
     it.ntiles = it.t1 > it.t0 ? (it.t1 - it.t0 + kTile - 1) / kTile : 0;
     return it;
 }
@@ -155,14 +157,16 @@ __device__ __forceinline__ void build(const DecodeParams &p, int *prefix, int *o
 constexpr int kTableItems = 512;       // items per CTA the table holds (8 KiB)
 
 __device__ __forceinline__ int4 pack_item(const Item &it) {
-    return make_int4(it.b | (it.kvh << 16), it.t0, it.t1, it.slot | (it.direct ? int(0x80000000u) : 0));
+    return make_int4(it.b | (it.kvh << 16), it.t0, it.t1 | (it.last ? int(0x80000000u) : 0),
+                     it.slot | (it.direct ? int(0x80000000u) : 0));
 }
 __device__ __forceinline__ Item unpack_item(int4 d) {
     Item it;
     it.b = d.x & 0xFFFF;
     it.kvh = (int)((unsigned)d.x >> 16);
     it.t0 = d.y;
-    it.t1 = d.z;
+    it.t1 = d.z & 0x7FFFFFFF;
+    it.last = d.z < 0;
     it.slot = d.w & 0x7FFFFFFF;
     it.direct = d.w < 0;
     it.part = 0;                     // not needed once the table is built

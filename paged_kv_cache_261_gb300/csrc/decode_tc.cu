@@ -127,6 +127,35 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// The decode step's own token of the item's sequence (position ctx - 1), for the
+// item's kv head, when the call carries it (decode with append). The producer warps
+// read its slot and its row (K by the K producer, V by the V producer) at the start
+// of the sequence's last item and write the row just before they load the item's
+// last tile, so that tile's loads read it. `e` is the block-table entry of the
+// token's block (the one that tile loads). The slot must be that of position
+// ctx - 1 (a different one sets PA_DEVERR_SLOT and is not written; -1 writes nothing).
+constexpr int kAppVecs = kD * 2 / 16;          // one kv head's row: 16 vectors of 16 bytes
+
+__device__ __forceinline__ uint4 append_row(const DecodeParams &p, const Item &I, bool is_v, int lane) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(is_v ? p.app_v : p.app_k) +
+                       ((int64_t)I.b * p.num_kv_heads + I.kvh) * kAppVecs;
+    return lane < kAppVecs ? src[lane] : make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void append_token(const DecodeParams &p, const Item &I, int slot, int e, uint4 row,
+                                             bool is_v, int lane) {
+    const int pos = I.t1 - 1;
+    const int64_t expect = (int64_t)e * p.block_size + (pos & (p.block_size - 1));
+    if (e < 0 || e >= p.num_blocks || (int64_t)slot != expect) {
+        if (!is_v && lane == 0) raise_error(p.err, PA_DEVERR_SLOT);
+        return;
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(const_cast<void *>(is_v ? p.value_cache : p.key_cache)) +
+                 ((int64_t)slot * p.num_kv_heads + I.kvh) * kAppVecs;
+    if (lane < kAppVecs) dst[lane] = row;
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // the tile's TMA loads read it
+}
+
 template <typename T> __device__ __forceinline__ uint16_t to_bits(float x);
 template <> __device__ __forceinline__ uint16_t to_bits<__nv_bfloat16>(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
@@ -241,12 +270,27 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         for (int k = 0; k < nmy && ok; ++k) {
             const Item I = decode_order::unpack_item(items[k]);
             const decode_order::ItemTable tb = decode_order::load_item_table(p, I, lane);
+            // decode with append: the slot of the sequence's new token, read here and
+            // used at the item's last tile (an empty context takes only -1)
+            int app_slot = -1;
+            uint4 app_row = make_uint4(0, 0, 0, 0);
+            if (p.app_slots != nullptr && I.last) {
+                app_slot = p.app_slots[I.b];
+                if (I.ntiles > 0) app_row = append_row(p, I, is_v, lane);
+            }
+            if (app_slot != -1 && I.ntiles == 0 && I.t1 == 0 && !is_v && lane == 0) raise_error(p.err, PA_DEVERR_SLOT);
             const int qrow = I.b * p.num_heads + I.kvh * G;
             for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
                 const int stage = it % kStages;
                 const uint32_t ph = (it / kStages) & 1;
                 bool live;
                 const int e = decode_order::tile_entry(tb, tile, nbt, lane, &live);
+                if (app_slot != -1 && tile == I.ntiles - 1) {
+                    // lane of the token's block among this tile's blocks
+                    const int jl = (((I.t1 - 1) >> p.log2_block_size) - (I.t0 >> p.log2_block_size)) - tile * nbt;
+                    append_token(p, I, app_slot, __shfl_sync(0xffffffffu, e, jl), app_row, is_v, lane);
+                    __syncwarp();
+                }
                 int phys = (int)p.num_blocks;           // out of range: TMA fills zeros
                 if (live) {
                     if (e >= 0 && e < p.num_blocks) phys = e;
@@ -636,6 +680,11 @@ int launch_decode_tc(const DecodeParams &p, int dtype, cudaStream_t stream) {
         c.block_tables = p.block_tables + (int64_t)b0 * p.max_blocks_per_seq;
         c.context_lens = p.context_lens + b0;
         if (p.prefix_lens) c.prefix_lens = p.prefix_lens + b0;
+        if (p.app_slots) {
+            c.app_slots = p.app_slots + b0;
+            c.app_k = static_cast<const char *>(p.app_k) + (int64_t)b0 * p.num_kv_heads * kD * 2;
+            c.app_v = static_cast<const char *>(p.app_v) + (int64_t)b0 * p.num_kv_heads * kD * 2;
+        }
         if (p.ws_ml) {
             c.ws_ml = p.ws_ml + rows * p.max_partitions * 2;
             c.ws_o = p.ws_o + rows * p.max_partitions * kD;

@@ -20,6 +20,12 @@ struct DecodeParams {
     float *ws_o;               // [B][H][P][D] unnormalised partial outputs
     unsigned int *err;         // device error word
     const int32_t *prefix_lens;  // optional [B]: leading tokens attended by the shared-prefix pass
+    // optional decode-step write (tensor-core kernel): sequence b's new token, rows
+    // app_k / app_v [B][Hk][128], goes to slot app_slots[b], which must be the slot of
+    // position ctx_b - 1; the CTA reading that block writes it first
+    const void *app_k;
+    const void *app_v;
+    const int32_t *app_slots;
     int64_t num_blocks;
     int max_blocks_per_seq;
     int num_seqs;

@@ -145,6 +145,17 @@ def test_write_fp8_rejects_bad_arguments(pa):
     assert L.pa_copy_blocks(16, 16, 16, 0, 8, 16, 8, 128, 3, None) == 0
 
 
+def test_decode_append_rejects_bad_arguments(pa):
+    L = pa.lib()
+
+    def call(k_new=16, v_new=16, slots=16, B=4):
+        return L.pa_paged_attention_decode_append(16, 16, k_new, v_new, slots, 16, 16, 16, 8, 16, B, 8, 2, 128, 16,
+                                                  64, 0.1, 0, 0, None, 0, 2, None)
+    assert call(B=0) == 0                # nothing to do
+    assert call(k_new=None) == -1 and call(slots=None) == -1
+    assert call(v_new=8) == -1           # misaligned
+
+
 def test_get_device_error_requires_output_pointer(pa):
     assert pa.lib().pa_get_device_error(None, None) == -1
 
