@@ -1,5 +1,6 @@
 """Decode with append (pa_paged_attention_decode_append) against the two calls it
-stands for: paged_kv_write of each sequence's new token, then the decode.
+stands for -- paged_kv_write of each sequence's new token, then the decode -- and
+against the oracle, in the launch configuration the bench times.
 
 Outputs and caches must be bit-identical to the separate calls: the tensor-core
 decode writes the tokens itself (the CTA that reads a token's block writes it
@@ -10,7 +11,7 @@ import pytest
 import torch
 
 import workloads
-from gpu_cases import dev, pa_mod
+from gpu_cases import assert_close, check_newest_rows, dev, oracle_decode, pa_mod, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +55,57 @@ def _both(pa, w, slots=None, partition_size=0):
         torch.cuda.synchronize()
         res.append((out, k2, v2, pa.get_device_error()))
     return res
+
+
+def _append(pa, w, max_context_len=0, partition_size=0):
+    """Decode with append over a NaN-poisoned cache that lacks each sequence's
+    newest token, in the launch configuration the bench uses (a workspace and the
+    host bound on the context length)."""
+    d = dev()
+    dt = workloads.torch_dtype(w.dtype)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    kc = torch.full(shape, float("nan"), dtype=dt, device=d)
+    vc = torch.full(shape, float("nan"), dtype=dt, device=d)
+    w.fill_cache_torch(kc, vc, include_newest=False)
+    kn, vn = w.newest_kv(like=kc)
+    q = w.q_values(like=kc).to(dt).contiguous()
+    out = torch.full_like(q, float("nan"))
+    mc = max_context_len or int(w.context_lens.max())
+    ws = torch.empty(max(pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, mc, partition_size), 16),
+                     dtype=torch.uint8, device=d)
+    pa.paged_attention_decode_append(out, q, kn.to(dt).contiguous(), vn.to(dt).contiguous(),
+                                     torch.as_tensor(w.slot_mapping, device=d), kc, vc,
+                                     torch.as_tensor(w.block_tables, device=d),
+                                     torch.as_tensor(w.context_lens, device=d), w.scale, max_context_len=mc,
+                                     partition_size=partition_size, workspace=ws)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+def test_append_ragged_against_the_oracle(pa):
+    ctx = np.array([1, 2, 127, 128, 129, 511, 512, 513, 1000, 3000, 77], np.int32)
+    w = workloads.make_decode("append_oracle", 606, ctx, 32, 8, 128, 16, "bf16")
+    out, kc, vc = _append(pa, w)
+    check_newest_rows(w, kc, vc)
+    assert_close(to_f64(out), oracle_decode(w, range(w.num_seqs)), "bf16", "append ragged")
+    assert pa.get_device_error() == 0
+
+
+def test_append_llama8b_full_batch_against_the_oracle(pa):
+    w = workloads.llama8b_decode()
+    out, kc, vc = _append(pa, w)
+    check_newest_rows(w, kc, vc)
+    assert_close(to_f64(out), oracle_decode(w, range(w.num_seqs)), "bf16", "append llama8b_decode")
+    assert pa.get_device_error() == 0
+
+
+def test_append_long_context_sampled_against_the_oracle(pa):
+    w = workloads.long_context()
+    out, kc, vc = _append(pa, w)
+    check_newest_rows(w, kc, vc)
+    seqs = [int(np.argmin(w.context_lens)), int(np.argmax(w.context_lens))]
+    assert_close(to_f64(out)[seqs], oracle_decode(w, seqs), "bf16", "append long_context")
+    assert pa.get_device_error() == 0
 
 
 def _same(a, b):
@@ -132,3 +184,4 @@ def test_append_reports_a_slot_that_is_not_the_last_position(pa):
     assert torch.equal(flat_k[int(bad[0])], flat_b[int(bad[0])])       # not written
     assert torch.equal(flat_k[int(bad[2])], flat_b[int(bad[2])])
     assert not torch.equal(flat_k[int(good[1])], flat_b[int(good[1])])  # the good token was
+
