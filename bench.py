@@ -376,7 +376,17 @@ class PrefillStep:
                 "query_tokens": pw.total_q, "chunk": self.max_q,
                 "prior_min": int((w.context_lens - pw.q_lens).min()),
                 "prior_max": int((w.context_lens - pw.q_lens).max()),
-                "l2": "K/V of the batch fit in L2 across a step; no flush (tensor-bound kernel)"}
+                "l2": self.l2_note()}
+
+    def l2_note(self):
+        w, pw = self.w, self.pw
+        mib = 2.0 ** 20
+        row = w.num_kv_heads * w.head_dim * 2
+        kv = int(w.context_lens.sum()) * row * 2
+        q = pw.total_q * w.num_heads * w.head_dim * 2
+        return (f"inputs larger than L2: {q / mib:.0f} MiB of queries + {kv / mib:.0f} MiB of K/V read per step "
+                f"(+ {q / mib:.0f} MiB of output and {pw.total_q * row * 2 / mib:.0f} MiB of chunk K/V written) "
+                f"vs {L2_BYTES / mib:.0f} MiB L2; no flush")
 
 
 # The kernel's own duration is taken from CUDA events around the call on every
