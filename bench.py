@@ -74,13 +74,41 @@ def base_workload(name: str):
             "mixed_serving": workloads.mixed_serving}[base], fp8
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed to one
+    space: what a compiler sees, so that a change to prose alone keeps a
+    kernel's recorded counters valid. String and character literals are kept
+    as written."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_digest(kernel: str = "decode_tc"):
+    """Digest of the code (comments and layout aside) of a kernel's sources."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_261_gb300", "csrc")
     for name in _KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,7 +1,7 @@
 // Work-item order shared by the persistent tensor-core decode kernels.
 //
-// A work item is (sequence, partition, kv head). Items are dealt to CTAs
-// round-robin in order of decreasing size: first every partition with the full
+// A work item is (sequence, partition, kv head). Items are dealt to CTAs in
+// serpentine rounds (below) in order of decreasing size: first every partition with the full
 // tile count (partition_size / 128 tiles: the full ones, and last partitions
 // just as long in tiles), then the other last partitions by tile count -- three
 // or more, two, one -- then empty contexts. prefix[] counts full-tile-count

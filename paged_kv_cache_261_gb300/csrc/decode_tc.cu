@@ -24,6 +24,9 @@
 //             end or with a bad id load from an out-of-range coordinate, which
 //             TMA fills with zeros.
 //   warp 7    TMA producer of V into the same stages (its own full barrier).
+//             In a decode with append, warps 0 and 7 also store the sequence's
+//             new K / V row just before they load the tile that holds it
+//             (append_token).
 //   warp 6    L2 prefetch: walks the same tiles up to kPrefetchTiles ahead of
 //             the producer's loads and pulls their blocks into L2.
 //   warp 1    S MMA issuer (one thread) and tensor-memory owner: S for tile i
@@ -37,9 +40,9 @@
 //             P^T to shared memory (bf16/f16, 128-byte swizzled K-major), zero
 //             V rows of masked tokens (their contents may be anything), and
 //             o = o * alpha + O_tile in registers.
-// Work items = (sequence, partition, kv head), dealt to CTAs round-robin in
-// order of decreasing size from a bucketed prefix sum that each CTA builds in
-// shared memory at kernel start (decode_order.cuh). Every wait is bounded (see
+// Work items = (sequence, partition, kv head), dealt to CTAs in serpentine
+// rounds in order of decreasing size, from a bucketed prefix sum that each CTA
+// builds in shared memory at kernel start (decode_order.cuh). Every wait is bounded (see
 // sm100.cuh); on a timeout the kernel sets PA_DEVERR_WAIT, drains its copies and
 // returns.
 #include <cuda.h>

@@ -1,0 +1,35 @@
+"""Host logic of bench.py that needs no GPU: the source digest that keys the
+committed DRAM-traffic records to the code they were measured on."""
+import json
+import os
+
+import bench
+
+CSRC = os.path.join(bench.ROOT, "paged_kv_cache_261_gb300", "csrc")
+
+
+def test_code_only_drops_comments_and_keeps_literals():
+    src = 'int a = 1; // one\n/* two\n lines */ const char *s = "x // y /* z */";\nchar c = \'/\';  int b;'
+    assert bench.code_only(src) == 'int a = 1; const char *s = "x // y /* z */"; char c = \'/\'; int b;'
+    assert bench.code_only('s = "q\\" // in"; // out') == 's = "q\\" // in";'
+    assert bench.code_only("x;// it's\ny;") == "x; y;"
+
+
+def test_prose_edits_keep_the_digest_and_code_edits_change_it():
+    with open(os.path.join(CSRC, "decode_tc.cu"), encoding="utf-8") as f:
+        text = f.read()
+    base = bench.code_only(text)
+    reworded = "// a new first line of prose\n" + text.replace("\n\n", "\n\n/* note */\n", 3)
+    assert bench.code_only(reworded) == base
+    changed = text.replace("constexpr int kStages = 3;", "constexpr int kStages = 4;")
+    assert changed != text and bench.code_only(changed) != base
+
+
+def test_every_traffic_record_names_a_kernel_family():
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    for wl, ent in rec.items():
+        assert ent["dram_bytes_per_launch"] > 0
+        assert len(ent["source_digest"]) == 16
+        fam = "decode_fp8" if wl.endswith("_fp8") else ("prefill_tc" if wl == "chunked_prefill" else "decode_tc")
+        assert fam in bench._KERNEL_SOURCES
