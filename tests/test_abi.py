@@ -171,3 +171,40 @@ def test_package_import_fails_loudly_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import paged_kv_cache_261_gb300"], cwd=tmp_path,
                        capture_output=True, text=True)
     assert r.returncode != 0 and "libpagedattn.so is missing" in r.stderr
+
+
+def test_every_compute_call_refuses_host_tensors(pa):
+    """No CPU fallback: each compute entry point rejects host tensors before any
+    work, and leaves its output untouched."""
+    import torch
+    B, H, Hk, D, bs, NB, MB = 2, 4, 2, 128, 16, 8, 4
+    kc = torch.zeros(NB, bs, Hk, D, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    kc8 = torch.zeros(NB, bs, Hk, D, dtype=torch.uint8)
+    vc8 = torch.zeros_like(kc8)
+    q = torch.ones(B, H, D, dtype=torch.bfloat16)
+    out = torch.full_like(q, 7.0)
+    kn = torch.zeros(B, Hk, D, dtype=torch.bfloat16)
+    vn = torch.zeros_like(kn)
+    slots = torch.tensor([0, 16], dtype=torch.int32)
+    bt = torch.arange(B * MB, dtype=torch.int32).view(B, MB)
+    cl = torch.tensor([1, 1], dtype=torch.int32)
+    qsl = torch.tensor([0, 1, 2], dtype=torch.int32)
+    pairs = torch.tensor([[0, 1]], dtype=torch.int32)
+    calls = {
+        "paged_kv_write": lambda: pa.paged_kv_write(kn, vn, slots, kc, vc),
+        "paged_attention_decode": lambda: pa.paged_attention_decode(out, q, kc, vc, bt, cl, 0.1),
+        "paged_attention_decode_append": lambda: pa.paged_attention_decode_append(out, q, kn, vn, slots, kc, vc, bt,
+                                                                                  cl, 0.1),
+        "paged_attention_prefill": lambda: pa.paged_attention_prefill(out, q, kc, vc, bt, cl, qsl, 0.1, 1),
+        "paged_attention_decode_shared": lambda: pa.paged_attention_decode_shared(
+            out, q, kc, vc, bt, cl, torch.zeros(B, dtype=torch.int32), torch.zeros(1, B, dtype=torch.int32), 0.1),
+        "copy_blocks": lambda: pa.copy_blocks(kc, vc, pairs),
+        "paged_kv_write_fp8": lambda: pa.paged_kv_write_fp8(kn, vn, slots, kc8, vc8, 1.0, 1.0),
+        "paged_attention_decode_fp8": lambda: pa.paged_attention_decode_fp8(out, q, kc8, vc8, bt, cl, 0.1, 1.0,
+                                                                            1.0),
+    }
+    for name, call in calls.items():
+        with pytest.raises(ValueError, match="must be a CUDA tensor"):
+            call()
+        assert torch.all(out == 7.0), name
