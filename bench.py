@@ -560,7 +560,10 @@ def cpu_baseline(w, fp8: bool = False, budget_s=15.0, min_time_s=10.0):
                       f"newest-token scatter + decode, {passes} passes in {dt:.1f} s"}
 
 
-def run_reference(args):
+def run_reference(args, budget_total_s: float = 90.0):
+    """The oracle, as it stands, on the host cores (the reference arm): each step
+    one pass over a prefix of the batch sized so that warm-up and timed steps
+    together take about budget_total_s."""
     import oracle
     name = args.workload
     if name not in DECODE_WORKLOADS + FP8_WORKLOADS:
@@ -568,7 +571,7 @@ def run_reference(args):
     build_w, fp8 = base_workload(name)
     w = build_w()
     threads = oracle.num_host_threads()
-    budget = 90.0 / max(args.steps + args.warmup, 1)
+    budget = budget_total_s / max(args.steps + args.warmup, 1)
     n = pick_sample(w, threads, budget, fp8)
     s = oracle_sample(w, n, fp8)
     for _ in range(args.warmup):

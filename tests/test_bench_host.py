@@ -33,3 +33,25 @@ def test_every_traffic_record_names_a_kernel_family():
         assert len(ent["source_digest"]) == 16
         fam = "decode_fp8" if wl.endswith("_fp8") else ("prefill_tc" if wl == "chunked_prefill" else "decode_tc")
         assert fam in bench._KERNEL_SOURCES
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    import argparse
+    args = argparse.Namespace(workload="llama8b_decode", steps=2, warmup=1, gpus=1)
+    bench.run_reference(args, budget_total_s=0.5)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    assert line["value"] > 0 and line["higher_is_better"] is True and line["steps"] == 2
+    assert line["config"]["workload"] == "llama8b_decode" and line["config"]["sampled_seqs"] >= 1
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    import sys
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"])
+    bench.main()
+    assert capsys.readouterr().out == ""
