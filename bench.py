@@ -154,13 +154,21 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) == 8:
-                    rows.append(parts)
+            lines = f.readlines()
         os.remove(self.path)
+        return self.summarise(lines)
+
+    @staticmethod
+    def summarise(lines):
+        """Median SM clock, the highest max clock and the throttle reasons seen
+        (any sample with the reason "Active") from the CSV samples; None if no
+        sample parsed."""
+        rows = []
+        for line in lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 8:
+                rows.append(parts)
         if not rows:
             return None
         sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]

@@ -55,3 +55,16 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"])
     bench.main()
     assert capsys.readouterr().out == ""
+
+
+def test_clock_samples_summary():
+    lines = ["2070, 2070, 812.3, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+             "2055, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+             "1980, 2070, 1401.2, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+             "[N/A], [N/A], [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]\n",
+             "garbage line\n"]
+    got = bench.ClockSampler.summarise(lines)
+    assert got == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 4}
+    hot = bench.ClockSampler.summarise(["1500, 2070, 1400, 0x48, Active, Active, Not Active, Not Active\n"])
+    assert hot["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+    assert bench.ClockSampler.summarise(["only, three, fields\n"]) is None
