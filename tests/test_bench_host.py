@@ -68,3 +68,37 @@ def test_clock_samples_summary():
     hot = bench.ClockSampler.summarise(["1500, 2070, 1400, 0x48, Active, Active, Not Active, Not Active\n"])
     assert hot["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
     assert bench.ClockSampler.summarise(["only, three, fields\n"]) is None
+
+
+def test_algorithmic_bytes_by_hand_on_the_tiny_batch():
+    import workloads
+    w = workloads.tiny_fp32()                       # contexts 5, 17, 33, 64; H = Hk = 4; D 64; bs 4; fp32
+    ab = w.algorithmic_bytes()
+    assert ab["kv"] == (5 + 17 + 33 + 64) * 4 * 64 * 2 * 4          # K and V once: 243,712 B
+    assert ab["qo"] == 2 * 4 * 4 * 64 * 4                           # q in, out back
+    assert ab["meta"] == 4 * (2 + 5 + 9 + 16) + 4 * 4               # table entries used, lengths
+    assert ab["decode"] == ab["kv"] + ab["qo"] + ab["meta"]
+    assert ab["write"] == 2 * 4 * 4 * 64 * (4 + 4) + 4 * 4          # one token per sequence, K and V
+    # an 8-bit cache counts one byte per cached element, the queries keep theirs
+    ab8 = w.algorithmic_bytes(cache_elem_bytes=1)
+    assert ab8["kv"] * 4 == ab["kv"] and ab8["qo"] == ab["qo"]
+
+
+def test_decode_bytes_of_the_8b_shaped_batch():
+    import workloads
+    w = workloads.llama8b_decode()
+    ab = w.algorithmic_bytes()
+    expect_kv = int(w.context_lens.astype("int64").sum()) * 8 * 128 * 2 * 2
+    assert ab["kv"] == expect_kv and 0.5e9 < ab["decode"] < 0.7e9   # about 0.6 GB a step
+
+
+def test_prefill_flops_by_brute_force():
+    import numpy as np
+    import workloads
+    pw = workloads.make_prefill("flops", 5, np.array([0, 3, 40], np.int32), np.array([4, 1, 7], np.int32),
+                                8, 2, 64, 16, "bf16")
+    visible = 0
+    for prior, n in [(0, 4), (3, 1), (40, 7)]:
+        for i in range(n):                          # query row i sits at position prior + i
+            visible += prior + i + 1                # and sees every key up to itself
+    assert pw.flops() == 4 * 64 * 8 * visible
