@@ -268,10 +268,13 @@ int pa_paged_attention_decode_append(void *out, const void *q, const void *k_new
         p.app_slots = slot_mapping;
         krc = pa::launch_decode_tc(p, dtype, s);
     } else {
-        // the scatter, then the decode
+        // the scatter, then the decode (head_dim 64 or 128 keeps a row a multiple of
+        // the scatter's 16-byte copies)
         const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * elem_size(dtype);
-        krc = pa::launch_kv_write(k_new, v_new, slot_mapping, num_seqs, key_cache, value_cache,
-                                  num_blocks * block_size, (int)row_bytes, p.err, s);
+        krc = row_bytes % 16 != 0 ? -2
+                                  : pa::launch_kv_write(k_new, v_new, slot_mapping, num_seqs, key_cache,
+                                                        value_cache, num_blocks * block_size, (int)row_bytes,
+                                                        p.err, s);
         if (krc == 0) krc = pa::launch_decode_simt(p, dtype, s);
     }
     if (krc == 0 && P > 1) krc = pa::launch_decode_reduce(p, dtype, s);
