@@ -102,3 +102,4 @@ def test_prefill_flops_by_brute_force():
         for i in range(n):                          # query row i sits at position prior + i
             visible += prior + i + 1                # and sees every key up to itself
     assert pw.flops() == 4 * 64 * 8 * visible
+
