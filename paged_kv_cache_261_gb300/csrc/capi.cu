@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include "../../include/pagedattn.h"
+#include "call_range.h"
 #include "common.cuh"
 #include "kernels.h"
 #include "kernels_fp8.h"
@@ -177,6 +178,7 @@ int pa_version(void) { return 100; }
 int pa_paged_kv_write(const void *k, const void *v, const int32_t *slot_mapping, int64_t num_tokens,
                       void *key_cache, void *value_cache, int64_t num_blocks, int block_size,
                       int num_kv_heads, int head_dim, int dtype, void *stream) {
+    const pa::CallRange range(__func__);
     const int es = elem_size(dtype);
     if (es == 0 || num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0)
@@ -213,6 +215,7 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
                               int64_t num_blocks, float scale, int max_context_len,
                               int partition_size, void *workspace, size_t workspace_bytes,
                               int dtype, void *stream) {
+    const pa::CallRange range(__func__);
     if (elem_size(dtype) == 0) return PA_ERR_INVALID_ARG;
     pa::DecodeParams p{};
     int64_t P = 0;
@@ -245,6 +248,7 @@ int pa_paged_attention_decode_append(void *out, const void *q, const void *k_new
                                      int head_dim, int block_size, int64_t num_blocks, float scale,
                                      int max_context_len, int partition_size, void *workspace,
                                      size_t workspace_bytes, int dtype, void *stream) {
+    const pa::CallRange range(__func__);
     if (elem_size(dtype) == 0) return PA_ERR_INVALID_ARG;
     pa::DecodeParams p{};
     int64_t P = 0;
@@ -287,6 +291,7 @@ int pa_paged_kv_write_fp8(const void *k, const void *v, const int32_t *slot_mapp
                           void *key_cache, void *value_cache, int64_t num_blocks, int block_size,
                           int num_kv_heads, int head_dim, float k_scale, float v_scale, int src_dtype,
                           void *stream) {
+    const pa::CallRange range(__func__);
     if (elem_size(src_dtype) == 0 || num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0)
         return PA_ERR_INVALID_ARG;
@@ -315,6 +320,7 @@ int pa_paged_attention_decode_fp8(void *out, const void *q, const void *key_cach
                                   int head_dim, int block_size, int64_t num_blocks, float scale, float k_scale,
                                   float v_scale, int max_context_len, int partition_size, void *workspace,
                                   size_t workspace_bytes, int dtype, void *stream) {
+    const pa::CallRange range(__func__);
     if (dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F16) return elem_size(dtype) ? PA_ERR_UNSUPPORTED
                                                                                   : PA_ERR_INVALID_ARG;
     if (!finite_positive(k_scale) || !finite_positive(v_scale)) return PA_ERR_INVALID_ARG;
@@ -355,6 +361,7 @@ int pa_paged_attention_decode_shared(void *out, const void *q, const void *key_c
                                      int head_dim, int block_size, int64_t num_blocks, float scale,
                                      int max_context_len, int partition_size, void *workspace,
                                      size_t workspace_bytes, int dtype, void *stream) {
+    const pa::CallRange range(__func__);
     if (elem_size(dtype) == 0 || num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
         num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
         max_blocks_per_seq <= 0 || max_context_len < 0 || partition_size < 0 || num_groups < 0 ||
@@ -464,6 +471,7 @@ int pa_paged_attention_prefill(void *out, const void *q, const void *key_cache, 
                                const int32_t *query_start_loc, int num_seqs, int64_t num_query_tokens,
                                int max_query_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
                                int64_t num_blocks, float scale, int dtype, void *stream) {
+    const pa::CallRange range(__func__);
     if (elem_size(dtype) == 0 || num_seqs < 0 || num_query_tokens < 0 || max_query_len < 0 || num_heads <= 0 ||
         num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks <= 0 || max_blocks_per_seq <= 0)
@@ -515,6 +523,7 @@ int pa_paged_attention_prefill(void *out, const void *q, const void *key_cache, 
 int pa_copy_blocks(void *key_cache, void *value_cache, const int32_t *src_dst_pairs, int64_t num_pairs,
                    int64_t num_blocks, int block_size, int num_kv_heads, int head_dim, int dtype,
                    void *stream) {
+    const pa::CallRange range(__func__);
     const int es = dtype == PA_DTYPE_E4M3 ? 1 : elem_size(dtype);
     if (es == 0 || num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0)
@@ -534,6 +543,7 @@ int pa_copy_blocks(void *key_cache, void *value_cache, const int32_t *src_dst_pa
 }
 
 int pa_get_device_error(void *stream, uint32_t *bits) {
+    const pa::CallRange range(__func__);
     if (!bits) return PA_ERR_INVALID_ARG;
     *bits = 0;
     unsigned int *err = nullptr;

@@ -21,6 +21,7 @@
 // order them.
 #include <stdint.h>
 
+#include "call_range.h"
 #include "../../include/pagedattn.h"
 #include "common.cuh"
 
@@ -59,6 +60,7 @@ int pa_paged_attention_decode_noalloc(void *out, const void *q, const void *key_
                                       int block_size, int64_t num_blocks, float scale,
                                       int max_context_len, int partition_size, int dtype,
                                       void *stream) {
+    const pa::CallRange range(__func__);
     if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size < 0 ||
         block_size <= 0 || max_blocks_per_seq <= 0)
         return PA_ERR_INVALID_ARG;
