@@ -435,6 +435,29 @@ int pa_alloc_refcount(const pa_allocator *a, int32_t block, int32_t *count);
 
 int pa_alloc_get_stats(const pa_allocator *a, pa_alloc_stats *out);
 
+/*
+ * Checkpoint / resume of the allocator's whole state: free stack (order
+ * included), reference counts, sequences with their lengths and tables, peak
+ * and copy counters. Not on the pages; a serving process that restarts keeps
+ * its device caches' block assignments.
+ *
+ * pa_alloc_snapshot writes an image of *a into buf (host memory, cap bytes) and
+ * its size into *size. With buf NULL it only reports the size; with cap below
+ * the size it writes nothing and returns PA_ERR_INVALID_ARG. The image is in
+ * host byte order, tagged "PAALLOC1".
+ *
+ * pa_alloc_restore builds a new allocator (*out, owned by the caller, freed
+ * with pa_alloc_destroy) from an image of exactly `size` bytes. It behaves as
+ * the allocator the image was taken from: the same blocks, in the same order,
+ * for every later call. The image is checked first. That means ids in range,
+ * the free stack exactly the blocks with count 0 (each once), every table as
+ * long as its length needs, every count at least the number of tables holding
+ * the block, sequence ids increasing, and no trailing bytes. Any failure
+ * returns PA_ERR_INVALID_ARG with *out = NULL.
+ */
+int pa_alloc_snapshot(const pa_allocator *a, void *buf, int64_t cap, int64_t *size);
+int pa_alloc_restore(const void *buf, int64_t size, pa_allocator **out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,6 +34,8 @@ _decl("pa_alloc_block", [_vp, ctypes.POINTER(ctypes.c_int32)])
 _decl("pa_alloc_decref", [_vp, ctypes.c_int32])
 _decl("pa_alloc_refcount", [_vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)])
 _decl("pa_alloc_get_stats", [_vp, ctypes.POINTER(_Stats)])
+_decl("pa_alloc_snapshot", [_vp, _vp, _i64, ctypes.POINTER(_i64)])
+_decl("pa_alloc_restore", [_vp, _i64, ctypes.POINTER(_vp)])
 
 
 @dataclass
@@ -118,6 +120,27 @@ class BlockAllocator:
         c = ctypes.c_int32(0)
         _ok(self._L.pa_alloc_refcount(self._h, block, ctypes.byref(c)), "pa_alloc_refcount")
         return int(c.value)
+
+    def snapshot(self) -> bytes:
+        """The allocator's whole state as bytes (see pa_alloc_snapshot)."""
+        n = _i64(0)
+        _ok(self._L.pa_alloc_snapshot(self._h, None, 0, ctypes.byref(n)), "pa_alloc_snapshot")
+        buf = ctypes.create_string_buffer(max(n.value, 1))
+        _ok(self._L.pa_alloc_snapshot(self._h, buf, n.value, ctypes.byref(n)), "pa_alloc_snapshot")
+        return buf.raw[: n.value]
+
+    @classmethod
+    def restore(cls, image: bytes) -> "BlockAllocator":
+        """A new allocator in the state a snapshot recorded (see pa_alloc_restore)."""
+        L = lib()
+        h = _vp()
+        data = bytes(image)
+        _ok(L.pa_alloc_restore(data, len(data), ctypes.byref(h)), "pa_alloc_restore")
+        self = cls.__new__(cls)
+        self._L, self._h = L, h
+        st = self.stats()
+        self.num_blocks, self.block_size = st.num_blocks, int.from_bytes(data[16:24], "little", signed=True)
+        return self
 
     def stats(self) -> AllocStats:
         s = _Stats()

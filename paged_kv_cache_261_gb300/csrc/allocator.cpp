@@ -14,6 +14,7 @@
 // append() is all-or-nothing.
 #include <algorithm>
 #include <cstdint>
+#include <cstring>
 #include <map>
 #include <new>
 #include <unordered_map>
@@ -69,6 +70,73 @@ struct pa_allocator {
         return (n > 0 && s.len % bs != 0 && ref[s.table[s.len / bs]] > 1) ? 1 : 0;
     }
 };
+
+// ---- checkpoint / resume ----------------------------------------------------
+// Image layout (host byte order; every field a little-endian integer on the
+// machines this builds for): 8-byte tag "PAALLOC1"; int64 num_blocks,
+// block_size, peak_used, cow_copies; int64 free count, then the free stack
+// bottom to top (int32 each); int32 reference count of every block; int64
+// sequence count, then per sequence in increasing id order: int64 id, int64
+// length, int64 table size, the table (int32 each).
+namespace {
+
+constexpr char kSnapTag[8] = {'P', 'A', 'A', 'L', 'L', 'O', 'C', '1'};
+
+struct Writer {
+    unsigned char *p;
+    int64_t n = 0;
+    template <typename T> void put(T v) {
+        if (p) std::memcpy(p + n, &v, sizeof v);
+        n += (int64_t)sizeof v;
+    }
+    void tag() {
+        if (p) std::memcpy(p + n, kSnapTag, sizeof kSnapTag);
+        n += (int64_t)sizeof kSnapTag;
+    }
+};
+
+struct Reader {
+    const unsigned char *p;
+    int64_t size, n = 0;
+    bool ok = true;
+    template <typename T> T get() {
+        T v{};
+        if (!ok || size - n < (int64_t)sizeof v) {
+            ok = false;
+            return v;
+        }
+        std::memcpy(&v, p + n, sizeof v);
+        n += (int64_t)sizeof v;
+        return v;
+    }
+};
+
+int64_t write_image(const pa_allocator *a, unsigned char *buf) {
+    Writer w{buf};
+    w.tag();
+    w.put<int64_t>(a->num_blocks);
+    w.put<int64_t>(a->block_size);
+    w.put<int64_t>(a->peak_used);
+    w.put<int64_t>(a->cow_copies);
+    w.put<int64_t>((int64_t)a->free_stack.size());
+    for (int32_t b : a->free_stack) w.put<int32_t>(b);
+    for (int32_t r : a->ref) w.put<int32_t>(r);
+    std::vector<int64_t> ids;
+    ids.reserve(a->seqs.size());
+    for (const auto &kv : a->seqs) ids.push_back(kv.first);
+    std::sort(ids.begin(), ids.end());
+    w.put<int64_t>((int64_t)ids.size());
+    for (int64_t id : ids) {
+        const Seq &s = a->seqs.find(id)->second;
+        w.put<int64_t>(id);
+        w.put<int64_t>(s.len);
+        w.put<int64_t>((int64_t)s.table.size());
+        for (int32_t b : s.table) w.put<int32_t>(b);
+    }
+    return w.n;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -236,6 +304,90 @@ int pa_alloc_get_stats(const pa_allocator *a, pa_alloc_stats *out) {
     out->peak_used = a->peak_used;
     out->num_cow_copies = a->cow_copies;
     out->num_seqs = (int64_t)a->seqs.size();
+    return PA_OK;
+}
+
+
+int pa_alloc_snapshot(const pa_allocator *a, void *buf, int64_t cap, int64_t *size) {
+    if (!a || !size || cap < 0) return PA_ERR_INVALID_ARG;
+    try {
+        *size = write_image(a, nullptr);
+        if (!buf) return PA_OK;
+        if (cap < *size) return PA_ERR_INVALID_ARG;
+        write_image(a, static_cast<unsigned char *>(buf));
+    } catch (...) {
+        return PA_ERR_OUT_OF_BLOCKS;
+    }
+    return PA_OK;
+}
+
+int pa_alloc_restore(const void *buf, int64_t size, pa_allocator **out) {
+    if (!out) return PA_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!buf || size < (int64_t)sizeof kSnapTag) return PA_ERR_INVALID_ARG;
+    if (std::memcmp(buf, kSnapTag, sizeof kSnapTag) != 0) return PA_ERR_INVALID_ARG;
+    Reader r{static_cast<const unsigned char *>(buf), size, (int64_t)sizeof kSnapTag};
+    pa_allocator *a = new (std::nothrow) pa_allocator();
+    if (!a) return PA_ERR_OUT_OF_BLOCKS;
+    int rc = PA_ERR_INVALID_ARG;
+    try {
+        const int64_t nb = r.get<int64_t>(), bs = r.get<int64_t>();
+        const int64_t peak = r.get<int64_t>(), copies = r.get<int64_t>(), nfree = r.get<int64_t>();
+        if (!r.ok || nb < 0 || nb > INT32_MAX || bs <= 0 || bs > INT32_MAX || copies < 0 || nfree < 0 ||
+            nfree > nb || (size - r.n) / 4 < nfree + nb)
+            throw rc;
+        a->num_blocks = nb;
+        a->block_size = (int)bs;
+        a->peak_used = peak;
+        a->cow_copies = copies;
+        a->free_stack.resize((size_t)nfree);
+        for (auto &b : a->free_stack) b = r.get<int32_t>();
+        a->ref.resize((size_t)nb);
+        for (auto &c : a->ref) c = r.get<int32_t>();
+        // the free stack is exactly the blocks nobody references, each once
+        std::vector<char> seen((size_t)nb, 0);
+        for (int32_t b : a->free_stack) {
+            if (b < 0 || b >= nb || seen[(size_t)b] || a->ref[(size_t)b] != 0) throw rc;
+            seen[(size_t)b] = 1;
+        }
+        int64_t zero = 0;
+        for (int32_t c : a->ref) {
+            if (c < 0) throw rc;
+            zero += c == 0;
+        }
+        if (zero != nfree || peak < a->used()) throw rc;
+        // sequences: increasing ids, tables as long as their lengths need, holding
+        // referenced blocks; a block's count covers at least the tables holding it
+        std::vector<int64_t> held((size_t)nb, 0);
+        const int64_t nseq = r.get<int64_t>();
+        if (!r.ok || nseq < 0 || (size - r.n) / 24 < nseq) throw rc;
+        int64_t prev = 0;
+        for (int64_t i = 0; i < nseq; ++i) {
+            const int64_t id = r.get<int64_t>(), len = r.get<int64_t>(), nt = r.get<int64_t>();
+            if (!r.ok || (i > 0 && id <= prev) || len < 0 || nt != (len + bs - 1) / bs || (size - r.n) / 4 < nt)
+                throw rc;
+            prev = id;
+            Seq s;
+            s.len = len;
+            s.table.resize((size_t)nt);
+            for (auto &b : s.table) {
+                b = r.get<int32_t>();
+                if (b < 0 || b >= nb || a->ref[(size_t)b] <= 0) throw rc;
+                held[(size_t)b] += 1;
+            }
+            a->seqs.emplace(id, std::move(s));
+        }
+        for (int64_t b = 0; b < nb; ++b)
+            if (held[(size_t)b] > a->ref[(size_t)b]) throw rc;
+        if (!r.ok || r.n != size) throw rc;
+    } catch (int) {
+        delete a;
+        return PA_ERR_INVALID_ARG;
+    } catch (...) {
+        delete a;
+        return PA_ERR_OUT_OF_BLOCKS;
+    }
+    *out = a;
     return PA_OK;
 }
 
