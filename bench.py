@@ -270,6 +270,9 @@ class Step:
         ab = w.algorithmic_bytes(cache_elem_bytes=ce)
         self.decode_bytes = ab["decode"]
         self.kv_bytes = ab["kv"]
+        self.decode_unique_bytes = self.decode_bytes
+        if self.unique_kv_bytes is not None:
+            self.decode_unique_bytes = self.decode_bytes - self.kv_bytes + self.unique_kv_bytes
         ntok = int(self.slots.shape[0])
         self.write_bytes = 2 * ntok * w.row_elems * (es + ce) + 4 * ntok
         self.step_bytes = self.decode_bytes + self.write_bytes + self.copy_bytes
@@ -334,17 +337,17 @@ class Step:
             pa.paged_attention_decode(self.out, q, self.kc, self.vc, bt, cl, self.w.scale,
                                       max_context_len=self.max_ctx, workspace=self.ws)
 
-    def run(self, ev=None):
-        """One step; ev = (start, end) CUDA events bracketing the decode call."""
+    def decode_call(self):
+        """The step's decode call alone (with its write when it is a decode with append)."""
+        self.decode(self.q, self.bt, self.cl, new=(self.k_new, self.v_new, self.slots) if self.append else None)
+
+    def run(self):
+        """One step: copy-on-write copies, the scatter of the new tokens, the decode."""
         if self.copy_pairs is not None:
             self.pa.copy_blocks(self.kc, self.vc, self.copy_pairs)
         if not self.append:
             self.write(self.k_new, self.v_new, self.slots)
-        if ev is not None:
-            ev[0].record()
-        self.decode(self.q, self.bt, self.cl, new=(self.k_new, self.v_new, self.slots) if self.append else None)
-        if ev is not None:
-            ev[1].record()
+        self.decode_call()
 
     def config(self):
         w = self.w
@@ -361,8 +364,15 @@ class Step:
                 "unique_kv_bytes": self.unique_kv_bytes,
                 "kv_cache": (f"e4m3 codes, k_scale = v_scale = {self.k_scale:.9g}" if self.fp8 else w.dtype),
                 "decode_kernel": "decode_fp8" if self.fp8 else os.environ.get("PA_DECODE_KERNEL", "auto"),
-                "l2": f"inputs larger than L2: {self.kv_bytes / 1e9:.2f} GB of K/V read per step "
-                      f"vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"}
+                "l2": self.l2_note()}
+
+    def l2_note(self):
+        mib = 2.0 ** 20
+        if self.unique_kv_bytes is not None:
+            return (f"{self.unique_kv_bytes / mib:.0f} MiB of unique K/V per step vs {L2_BYTES / mib:.0f} MiB L2: "
+                    f"steps run back to back (no flush); the decode roofline times each call after an L2 flush")
+        return (f"inputs larger than L2: {self.kv_bytes / 1e9:.2f} GB of K/V read per step "
+                f"vs {L2_BYTES / mib:.0f} MiB L2; no flush")
 
 
 class PrefillStep:
@@ -395,15 +405,13 @@ class PrefillStep:
         self.launches_per_step = 2
         torch.cuda.synchronize()
 
-    def run(self, ev=None):
-        pa = self.pa
-        pa.paged_kv_write(self.k_new, self.v_new, self.slots, self.kc, self.vc)
-        if ev is not None:
-            ev[0].record()
-        pa.paged_attention_prefill(self.out, self.q, self.kc, self.vc, self.bt, self.cl, self.qs, self.w.scale,
-                                   self.max_q)
-        if ev is not None:
-            ev[1].record()
+    def prefill(self):
+        self.pa.paged_attention_prefill(self.out, self.q, self.kc, self.vc, self.bt, self.cl, self.qs,
+                                        self.w.scale, self.max_q)
+
+    def run(self):
+        self.pa.paged_kv_write(self.k_new, self.v_new, self.slots, self.kc, self.vc)
+        self.prefill()
 
     def config(self):
         w, pw = self.w, self.pw
@@ -425,63 +433,130 @@ class PrefillStep:
                 f"vs {L2_BYTES / mib:.0f} MiB L2; no flush")
 
 
-# The kernel's own duration is taken from CUDA events around the call on every
-# TIMING_EVERY-th timed step (the first included). An event recorded between two
-# launches ends the programmatic overlap of the next kernel's set-up with the one
-# before (~7 us a step on the 8B-shaped decode), so the other steps run without
-# them and the step rate is not held back by its own measurement.
-TIMING_EVERY = 8
+# ---------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------
+
+SETTLE_S = 0.3          # warm-up wall time while the clock sampler starts
+KERNEL_WARM = 10        # untimed calls before a kernel-timing loop
+KERNEL_RUNS = 5         # event-bracketed runs of back-to-back calls
+KERNEL_CALLS = 50       # calls per run
+BRACKETED_CALLS = 50    # individually bracketed calls (upper-bound cross-check)
 
 
-def timed_events(torch, steps):
-    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range((steps + TIMING_EVERY - 1) // TIMING_EVERY)]
+def warm_up(torch, step, warmup: int, min_s: float = SETTLE_S) -> int:
+    """At least `warmup` untimed steps, continuing until min_s of wall time has
+    passed so that clocks have settled under load when the timed region starts
+    (the clock sampler starts meanwhile, with the GPU busy rather than idle).
+    Returns the number of warm-up steps run."""
+    n = 0
+    t = time.perf_counter()
+    while n < warmup or time.perf_counter() - t < min_s:
+        for _ in range(8):
+            step()
+            n += 1
+        torch.cuda.synchronize()
+    return n
+
+
+def time_calls(torch, call, runs: int = KERNEL_RUNS, calls: int = KERNEL_CALLS, warm: int = KERNEL_WARM):
+    """Device time of one call in steady state: `warm` untimed calls, then `runs`
+    runs of `calls` back-to-back calls, each run between two CUDA events on the
+    launching stream. Returns (median over the runs of ms per call, calls timed)."""
+    for _ in range(warm):
+        call()
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(runs):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(calls):
+            call()
+        b.record()
+        b.synchronize()
+        per.append(a.elapsed_time(b) / calls)
+    return statistics.median(per), runs * calls
+
+
+def time_calls_bracketed(torch, call, n: int = BRACKETED_CALLS, flush=None):
+    """Median ms of `n` calls each bracketed alone by two CUDA events (so none
+    overlaps its predecessor's tail). flush: a uint8 CUDA buffer larger than L2,
+    overwritten before every call so that no call finds its inputs in L2."""
+    evs = []
+    for _ in range(n):
+        if flush is not None:
+            flush.fill_(0x5A)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(x.elapsed_time(y) for x, y in evs)
+
+
+def l2_flush_buffer(torch, device):
+    return torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+
+
+def checked_roofline(achieved: float, peak: float, kernel_ms: float, ms_per_step: float, tol: float = 1.05):
+    """frac, or None with the reason, when the kernel time or the rate is not
+    physically consistent with the step it sits in."""
+    if kernel_ms > tol * ms_per_step:
+        return None, f"kernel time {kernel_ms:.4f} ms exceeds the step's {ms_per_step:.4f} ms"
+    if achieved > 1.2 * peak:
+        return None, f"achieved {achieved:.0f} above 1.2 x peak {peak:.0f}"
+    return achieved / peak, None
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except Exception:
+        return {}
 
 
 def run_prefill(args, device, rank, world):
     """Timed loop of the chunked-prefill step (TFLOP/s of causal attention)."""
     import torch
     st = PrefillStep(device)
-    for _ in range(max(args.warmup, 3)):
-        st.run()
+    st.run()
     torch.cuda.synchronize()
     if st.pa.get_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
-    evs = timed_events(torch, args.steps)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(None) if rank == 0 else None
-    if sampler is not None:
-        time.sleep(0.3)
+    nwarm = warm_up(torch, st.run, max(args.warmup, 3))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0.record()
-    for i in range(args.steps):
-        st.run(evs[i // TIMING_EVERY] if i % TIMING_EVERY == 0 else None)
+    for _ in range(args.steps):
+        st.run()
     t1.record()
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler is not None else None
     ms = max_over_ranks(t0.elapsed_time(t1), device) / args.steps
-    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except Exception:
-        pass
+    kern_ms, ncalls = time_calls(torch, st.prefill)
+    peaks = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
     achieved = st.flops / (kern_ms * 1e-3) / 1e12
+    frac, why = checked_roofline(achieved, peak, kern_ms, ms)
     line = {"metric": "paged chunked-prefill attention TFLOP/s on 1×GB300 (causal, packed chunks)",
             "value": world * st.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "steps": args.steps, "warmup": nwarm, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": st.w.dtype, "data": "synthetic",
             "config": st.config(), "tokens_per_s": world * st.pw.total_q / (ms * 1e-3),
             "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
                          "peak_kind": "measured bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks
-                         else "fallback", "unit": "TFLOP/s", "frac": achieved / peak,
+                         else "fallback", "unit": "TFLOP/s", "frac": frac,
                          "algorithmic_flops_per_launch": st.flops, "kernel_ms": kern_ms,
-                         "timed_launches": len(evs),
-                         "timing": f"CUDA events around the prefill call on every {TIMING_EVERY}th timed step",
+                         "timed_launches": ncalls,
+                         "timing": f"median over {KERNEL_RUNS} event-bracketed runs of {KERNEL_CALLS} back-to-back "
+                                   f"prefill calls, after the timed steps",
                          "traffic": recorded_traffic("chunked_prefill", "prefill_tc")},
             "gpu_launches": st.launches_per_step * args.steps, "clocks": clocks}
+    if why:
+        line["roofline"]["frac_null_reason"] = why
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -627,74 +702,141 @@ def run_ours(args):
             dist.destroy_process_group()
         return
     st = Step(args.workload, device)
-    for _ in range(max(args.warmup, 3)):
-        st.run()
+    st.run()
     torch.cuda.synchronize()
     if st.pa.get_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
-    evs = timed_events(torch, args.steps)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
     except Exception:
         pass
     sampler = ClockSampler(gpu_id) if rank == 0 else None
-    if sampler is not None:
-        time.sleep(0.3)
+    nwarm = warm_up(torch, st.run, max(args.warmup, 3))
     if world > 1:
         dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0.record()
-    for i in range(args.steps):
-        st.run(evs[i // TIMING_EVERY] if i % TIMING_EVERY == 0 else None)
+    for _ in range(args.steps):
+        st.run()
     t1.record()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler is not None else None
-    ms = t0.elapsed_time(t1)
-    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    ms = max_over_ranks(ms, device)
+    ms = max_over_ranks(t0.elapsed_time(t1), device)
     ms_step = ms / args.steps
+    if st.pa.get_device_error() != 0:
+        raise RuntimeError("device error word set during the timed steps")
+
+    # the decode call's own device time, after the timed steps
+    peak, peak_kind = hbm_peak()
+    roof = decode_roofline(torch, st, device, peak, peak_kind, ms_step)
 
     # end to end through the public API: pinned host inputs in, result out, every step
     e2e = run_e2e(st, args, device)
+    w = st.w
+    secondary = []
+    if not args.no_secondary and args.workload == "llama8b_decode":
+        # the other configuration the 70 % target names, measured in the same run
+        del st
+        torch.cuda.empty_cache()
+        secondary.append(secondary_record(torch, "long_context", device, peak, peak_kind))
+        torch.cuda.empty_cache()
+        st = None
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
-    peak, peak_kind = hbm_peak()
-    achieved = st.decode_bytes / (decode_ms * 1e-3) / 1e9
-    value = job_gbs(world, st.step_bytes, ms_step)
-    w = st.w
+    step_bytes, config, launches = roof.pop("_step_bytes"), roof.pop("_config"), roof.pop("_launches_per_step")
+    value = job_gbs(world, step_bytes, ms_step)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": nwarm, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded counter-based generator)",
-        "config": st.config(),
+        "config": config,
         "tokens_per_s": world * w.num_seqs / (ms_step * 1e-3),
         "kv_tokens_per_s": world * int(w.context_lens.sum()) / (ms_step * 1e-3),
         "hbm_fraction": value / world / peak,
-        "roofline": {"kernel": "paged_attention_decode (partition + merge kernels)", "bound": "hbm",
-                     "achieved": achieved, "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs",
-                     "unit": "GB/s", "frac": achieved / peak,
-                     "algorithmic_bytes_per_launch": st.decode_bytes,
-                     "decode_ms": decode_ms,
-                     "timed_launches": len(evs),
-                     "timing": f"CUDA events around the decode call on every {TIMING_EVERY}th timed step",
-                     "traffic": recorded_traffic(args.workload, "decode_fp8" if st.fp8 else "decode_tc")},
+        "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": st.launches_per_step * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
     }
+    if secondary:
+        line["secondary"] = secondary
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, st.fp8)
+        line["cpu_baseline"] = cpu_baseline(w, args.workload.endswith("_fp8"))
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def decode_roofline(torch, st: "Step", device, peak: float, peak_kind: str, ms_step: float | None):
+    """Roofline of the decode call of a step: algorithmic bytes per call over its
+    device time in steady state (back-to-back calls), checked against the step
+    time. For the shared-prefix workload the bytes are the unique bytes (each
+    shared block once) and every call is timed alone after an L2 flush, so that
+    no call finds the previous call's blocks in L2."""
+    shared = st.shared is not None
+    if shared:
+        flush = l2_flush_buffer(torch, device)
+        for _ in range(KERNEL_WARM):
+            st.decode_call()
+        kern_ms = time_calls_bracketed(torch, st.decode_call, flush=flush)
+        ncalls, bracketed = BRACKETED_CALLS, kern_ms
+        timing = (f"median of {BRACKETED_CALLS} decode calls, each between its own two CUDA events after an "
+                  f"L2 flush (a {2 * L2_BYTES >> 20} MiB write)")
+        del flush
+        bytes_ = st.decode_unique_bytes
+    else:
+        kern_ms, ncalls = time_calls(torch, st.decode_call)
+        bracketed = time_calls_bracketed(torch, st.decode_call)
+        timing = (f"median over {KERNEL_RUNS} runs of {KERNEL_CALLS} back-to-back decode calls, each run between "
+                  f"two CUDA events on the launching stream, after the timed steps")
+        bytes_ = st.decode_bytes
+    achieved = bytes_ / (kern_ms * 1e-3) / 1e9
+    ref_ms = ms_step if ms_step is not None else kern_ms
+    frac, why = checked_roofline(achieved, peak, kern_ms, ref_ms)
+    kernel = ("decode_fp8_kernel + merge" if st.fp8 else
+              "shared-prefix pass + private decode_tc_kernel pass + merge" if shared else
+              "decode call: decode_tc_kernel (partitions; writes the new tokens) + merge")
+    roof = {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peak,
+            "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": frac,
+            "algorithmic_bytes_per_launch": bytes_, "decode_ms": kern_ms, "timed_launches": ncalls,
+            "timing": timing, "decode_ms_bracketed_median": bracketed,
+            "traffic": recorded_traffic(st.name, "decode_fp8" if st.fp8 else "decode_tc")}
+    if shared:
+        roof["logical_bytes_per_launch"] = st.decode_bytes
+        roof["bytes"] = "unique: every shared prefix block counted once per group"
+    if why:
+        roof["frac_null_reason"] = why
+    roof["_step_bytes"] = st.step_bytes
+    roof["_config"] = st.config()
+    roof["_launches_per_step"] = st.launches_per_step
+    return roof
+
+
+def secondary_record(torch, name: str, device, peak: float, peak_kind: str):
+    """The decode roofline of another workload, measured in the same run."""
+    st = Step(name, device)
+    st.run()
+    torch.cuda.synchronize()
+    if st.pa.get_device_error() != 0:
+        raise RuntimeError(f"device error word set on {name}")
+    roof = decode_roofline(torch, st, device, peak, peak_kind, None)
+    for k in ("_step_bytes", "_launches_per_step"):
+        roof.pop(k)
+    cfg = roof.pop("_config")
+    roof = {"workload": name, "config": {k: cfg[k] for k in ("num_seqs", "num_heads", "num_kv_heads", "head_dim",
+                                                             "block_size", "context_total", "context_min",
+                                                             "context_max", "partition_size", "kv_cache", "l2")},
+            **roof}
+    del st
+    return roof
 
 
 def run_e2e(st: Step, args, device):
@@ -709,7 +851,7 @@ def run_e2e(st: Step, args, device):
     to finish reading it; that decode's output is on the host before step i + 2
     writes output buffer j again)."""
     import torch
-    n = max(min(args.steps, 500), 10)
+    n = min(max(args.steps, 200), 2000)
     items = [("q", st.q), ("k", st.k_new), ("v", st.v_new), ("slots", st.slots), ("bt", st.bt), ("cl", st.cl)]
     if st.shared is not None:
         items += [("pl", st.shared[0]), ("gm", st.shared[1])]
@@ -796,6 +938,8 @@ def main():
     ap.add_argument("--workload", default="llama8b_decode",
                     choices=[*DECODE_WORKLOADS, *FP8_WORKLOADS, "shared_prefix", "chunked_prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the long-context decode record that the 8B-shaped run adds")
     args = ap.parse_args()
     if args.impl == "reference":
         if int(os.environ.get("RANK", "0")) != 0:

@@ -351,6 +351,25 @@ int pa_paged_attention_decode_fp8(void *out, const void *q, const void *key_cach
  */
 int pa_get_device_error(void *stream, uint32_t *bits);
 
+/*
+ * Check of the failure path of the pipeline kernels' waits. The pages have no
+ * counterpart; it tests this library's own failure detection.
+ *
+ * Every wait of the tensor-core kernels on an mbarrier is bounded: after a
+ * limit of real time (1 s in those kernels) it gives up, the whole warp agrees
+ * on that, and the kernel sets PA_DEVERR_WAIT, drains and returns instead of
+ * hanging. This call runs that same wait code in a one-warp kernel on an
+ * mbarrier phase that nothing completes, with nothing in flight, after first
+ * completing and observing one phase itself. The wait gives up after limit_ns
+ * nanoseconds (1000 <= limit_ns <= 1e9, else PA_ERR_INVALID_ARG) and the kernel
+ * sets PA_DEVERR_WAIT in the device error word (read it with
+ * pa_get_device_error). report, if not NULL, is device memory of 4 int64
+ * (8-byte aligned): [0] 1 if the completed phase was seen, [1] how many of the
+ * 32 lanes gave up on their own wait, [2] 1 if the warp agreed on the failure,
+ * [3] nanoseconds lane 0 waited before giving up. Asynchronous on `stream`.
+ */
+int pa_check_bounded_wait(int64_t limit_ns, int64_t *report, void *stream);
+
 /* ---- host block allocator ------------------------------------------------- */
 /*
  * [P1 PagedKVManager: block pool whose free ids sit on a stack (initially

@@ -81,6 +81,7 @@ _decl("pa_paged_attention_decode_append", [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _v
                                            _i32, _i32, _i64, _f, _i32, _i32, _vp, _sz, _i32, _vp])
 _decl("pa_copy_blocks", [_vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp])
 _decl("pa_get_device_error", [_vp, ctypes.POINTER(ctypes.c_uint32)])
+_decl("pa_check_bounded_wait", [_i64, _vp, _vp])
 _decl("pa_decode_shared_workspace_bytes", [_i32, _i32, _i32, _i32, _i32], _sz)
 _decl("pa_paged_attention_decode_shared", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                            _i32, _i32, _i32, _i32, _i64, _f, _i32, _i32, _vp, _sz, _i32, _vp])
@@ -482,6 +483,22 @@ def get_device_error(stream=None, device=None) -> int:
     if rc not in (PA_OK, PA_ERR_DEVICE_INDEX):
         raise PagedAttnError(rc, "pa_get_device_error")
     return int(bits.value)
+
+
+def check_bounded_wait(limit_ns: int, report=None, stream=None) -> None:
+    """Run the bounded-wait failure check (pa_check_bounded_wait): one warp waits
+    limit_ns on an mbarrier phase nothing completes, then sets PA_DEVERR_WAIT.
+    report: optional int64 CUDA tensor of 4 elements (see the C header)."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ptr = None
+    if report is not None:
+        report = _cuda(report, "report", dtype=torch.int64)
+        if report.numel() < 4:
+            raise ValueError("report needs 4 int64 elements")
+        dev = report.device
+        ptr = report.data_ptr()
+    _check(_lib.pa_check_bounded_wait(int(limit_ns), ptr, _stream_ptr(stream, dev)), "pa_check_bounded_wait")
 
 
 from .allocator import AllocStats, BlockAllocator  # noqa: E402,F401

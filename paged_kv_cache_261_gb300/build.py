@@ -24,7 +24,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
 
 SOURCES = ["capi.cu", "kv_write.cu", "kv_write_fp8.cu", "decode_simt.cu", "decode_tc.cu", "decode_fp8.cu",
-           "prefill_tc.cu", "decode_noalloc.cu", "allocator.cpp"]
+           "prefill_tc.cu", "decode_noalloc.cu", "selftest.cu", "allocator.cpp"]
 
 
 def _nvcc() -> str:

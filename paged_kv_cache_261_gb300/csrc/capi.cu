@@ -542,6 +542,18 @@ int pa_copy_blocks(void *key_cache, void *value_cache, const int32_t *src_dst_pa
     return PA_OK;
 }
 
+int pa_check_bounded_wait(int64_t limit_ns, int64_t *report, void *stream) {
+    const pa::CallRange range(__func__);
+    if (limit_ns < 1000 || limit_ns > 1000000000) return PA_ERR_INVALID_ARG;
+    if (report && (reinterpret_cast<uintptr_t>(report) & 7u) != 0) return PA_ERR_INVALID_ARG;
+    unsigned int *err = nullptr;
+    if (int rc = error_word(&err)) return rc;
+    if (pa::launch_bounded_wait_check((unsigned long long)limit_ns, report, err,
+                                      static_cast<cudaStream_t>(stream)) != 0)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
 int pa_get_device_error(void *stream, uint32_t *bits) {
     const pa::CallRange range(__func__);
     if (!bits) return PA_ERR_INVALID_ARG;

@@ -132,4 +132,9 @@ int launch_decode_tc(const DecodeParams &p, int dtype, cudaStream_t stream);
 // Merge of the partials of sequences with more than one partition.
 int launch_decode_reduce(const DecodeParams &p, int dtype, cudaStream_t stream);
 
+// One warp waiting on an mbarrier phase that nothing completes, with the
+// pipeline kernels' bounded wait (selftest.cu).
+int launch_bounded_wait_check(unsigned long long limit_ns, int64_t *report, unsigned int *err,
+                              cudaStream_t stream);
+
 }  // namespace pa

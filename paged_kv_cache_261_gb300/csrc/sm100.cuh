@@ -49,13 +49,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait for the phase with the given parity to complete; false on timeout.
-// (In code where the whole warp continues together, use warp_wait.)
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false once limit_ns of
+// real time have passed without it. (In code where the whole warp continues
+// together, use warp_wait.)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return true;
 }
@@ -63,8 +65,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
 // Every lane waits (bounded), then the warp agrees: all lanes see the same
 // outcome, so a timeout never leaves lanes diverged before a warp-collective
 // instruction.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
 }
 
 // ---- TMA ---------------------------------------------------------------------

@@ -40,6 +40,14 @@ def test_library_exports_every_declared_symbol(pa):
     assert missing == []
 
 
+def test_bounded_wait_check_validates_on_the_host(pa):
+    # refused before any CUDA call: a bound outside [1 us, 1 s], a misaligned report
+    L = pa.lib()
+    assert L.pa_check_bounded_wait(0, None, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_check_bounded_wait(2_000_000_000, None, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_check_bounded_wait(1_000_000, 12, None) == pa.PA_ERR_INVALID_ARG
+
+
 def test_status_strings(pa):
     assert pa.status_string(0) == "PA_OK"
     assert pa.status_string(-5) == "PA_ERR_DEVICE_INDEX"

@@ -8,14 +8,17 @@ consume what it makes; neither is imported here.
 
 Token contents come from a counter-based generator. Element ``e`` of the row that
 tensor ``tid`` (K, V or q) holds for content key ``key`` at position ``pos`` is a
-pure integer function of ``(seed, tid, key, pos, e)``. The value is the sum of
-twelve 4-bit uniforms, centred and divided by 16: an Irwin-Hall stand-in for
-N(0, 1) with standard deviation 0.998 and range [-5.625, 5.625]. Every value is a
-multiple of 1/16 with at most 7 significant bits, so it is exact in fp32, fp16 and
-bf16 and the storage dtype needs no rounding step. The same code runs on numpy
-arrays and on torch tensors (host or device) and yields identical bits on both,
-which lets a test regenerate on the host exactly the rows that were generated on
-the device.
+pure integer function of ``(seed, tid, key, pos, e)``: the centred sum of twelve
+independent uniforms on [0, 1), an Irwin-Hall stand-in for N(0, 1) (standard
+deviation 0.998, range about +-5.66). Eleven of the uniforms carry 4 bits and
+one carries 20, so the sum is continuous to 2^-21 and a value has up to 24
+significant bits: it is an exact float32 (the fp32 workloads use it as it is)
+with a full mantissa, and the 16-bit workloads store it rounded to nearest-even
+in fp16 or bf16 -- the same rounding on both sides (``to_storage_numpy`` here,
+torch's casts on the device), so the oracle reads exactly the values the GPU
+reads. The integer code runs on numpy arrays and on torch tensors (host or
+device) and yields identical bits on both, which lets a test regenerate on the
+host exactly the rows that were generated on the device.
 
 Shapes follow the cache layout ``[num_blocks, block_size, num_kv_heads,
 head_dim]``. A table entry of -1 marks an unused logical block.
@@ -61,8 +64,17 @@ def _mix_scalar(v: int) -> int:
     return (v >> 16) ^ v
 
 
+# Largest magnitude content_rows can return: 11862015 / 2**21.
+CONTENT_MAX = 11862015.0 / 2097152.0
+
+
 def _irwin_hall(keys):
-    """keys: int64 array in [0, 2**32). Returns float32 values in [-5.625, 5.625]."""
+    """keys: int64 array in [0, 2**32). Returns float32 values in [-CONTENT_MAX, CONTENT_MAX].
+
+    Twelve uniforms on [0, 1): eleven 4-bit ones (nibbles of two hashes) and one
+    20-bit one (a nibble of the first hash extended by the second hash's top 16
+    bits). Their sum minus its mean is n / 2**21 for an odd integer n with
+    |n| <= 11862015 < 2**24, so the float32 conversion and the scaling are exact."""
     a = _mix32(keys)
     b = _mix32(keys ^ 0x5BD1E995)
     s = a & 15
@@ -70,11 +82,12 @@ def _irwin_hall(keys):
         s = s + ((a >> (4 * i)) & 15)
     for i in range(4):
         s = s + ((b >> (4 * i)) & 15)
-    s = s - 90
-    if _is_torch(s):
+    f = b >> 16
+    n = 2 * (s * 65536 + f) - (180 * 65536 + 65535)
+    if _is_torch(n):
         import torch
-        return s.to(torch.float32) / 16.0
-    return s.astype(np.float32) / np.float32(16.0)
+        return n.to(torch.float32) / 2097152.0
+    return n.astype(np.float32) / np.float32(2097152.0)
 
 
 def content_rows(seed: int, tid: int, keys, positions, row_elems: int):
@@ -101,7 +114,7 @@ def content_codes(seed: int, tid: int, keys, positions, row_elems: int):
     random sign, a random 3-bit mantissa and an exponent field drawn uniformly
     from {0 (subnormal), 4, 5, ..., 14}: magnitudes from 2^-9 to 240, never the
     NaN pattern. With a scale of 5.625 / 448 the decoded values span about
-    [-3, 3], the range of the float rows. No quantisation is involved.
+    [-3, 3], inside the range of the float rows. No quantisation is involved.
     """
     h = _mix_scalar(seed * 0x9E3779B1 + tid * 0x7FEB352D + 0x3C6EF372)
     r = _mix32(((_mix32((keys + h) & M32)) + positions * 0x2C1B3C6D) & M32)
@@ -121,35 +134,51 @@ def content_codes(seed: int, tid: int, keys, positions, row_elems: int):
     return code.astype(np.uint8)
 
 
-FP8_SCALE = 5.625 / 448.0     # float rows span [-5.625, 5.625]; that maps them onto [-448, 448]
+FP8_SCALE = 5.625 / 448.0     # maps [-5.625, 5.625] onto [-448, 448]; rarer larger rows saturate
 
 
 # ---------------------------------------------------------------------------
-# bf16 / f16 storage helpers (bit containers; values are already exact)
+# bf16 / f16 storage helpers (round to nearest even, as torch's casts do)
 # ---------------------------------------------------------------------------
+
+def _bf16_bits_rne(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns, round to nearest with ties to even; any NaN
+    becomes 0x7FC0 (torch's canonical bf16 NaN). Infinities and overflow follow
+    from the same carry."""
+    u = x.view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    out = r.astype(np.uint16)
+    out[np.isnan(x)] = 0x7FC0
+    return out
+
 
 def to_storage_numpy(x: np.ndarray, dtype: str) -> np.ndarray:
-    """float32 values (exact in the target dtype) -> numpy array holding the bits.
-
-    f32 -> float32, f16 -> float16, bf16 -> uint16 bit patterns."""
+    """float32 values -> numpy array holding them in the storage dtype, rounded
+    to nearest even: f32 -> float32 (unchanged), f16 -> float16, bf16 -> uint16
+    bit patterns."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     if dtype == "f32":
         return x
     if dtype == "f16":
-        return x.astype(np.float16)
+        with np.errstate(over="ignore"):
+            return x.astype(np.float16)
     if dtype == "bf16":
-        u = x.view(np.uint32)
-        if np.any(u & 0xFFFF):
-            raise ValueError("value not exactly representable in bf16")
-        return (u >> 16).astype(np.uint16)
+        return _bf16_bits_rne(x)
     raise ValueError(dtype)
 
 
 def storage_to_float64(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Inverse of to_storage_numpy (exact)."""
+    """Inverse of to_storage_numpy on stored values (exact)."""
     if dtype == "bf16":
         return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return x.astype(np.float64)
+
+
+def rounded(x, dtype: str):
+    """float32 values as the storage dtype holds them (numpy or torch input)."""
+    if _is_torch(x):
+        return x.to(torch_dtype(dtype)).float()
+    return storage_to_float64(to_storage_numpy(x, dtype), dtype).astype(np.float32)
 
 
 def torch_dtype(dtype: str):
@@ -233,7 +262,7 @@ class DecodeWorkload:
         return self.kv_codes(tid, seq_idx, positions) if codes else self.kv_rows(tid, seq_idx, positions)
 
     def q_values(self, like=None):
-        """float32 [B, H, D] queries (q_mult applied; exact in every dtype)."""
+        """float32 [B, H, D] queries (q_mult applied; callers round to the storage dtype)."""
         B, H, D = self.num_seqs, self.num_heads, self.head_dim
         if like is not None and _is_torch(like):
             import torch
