@@ -69,9 +69,20 @@ constexpr int kChunkBytes = kTile * 128;          // 128 rows x 64 dims x 2 B
 constexpr int kKVBytes = 2 * kChunkBytes;         // one tile of K (or V), both 64-dim halves
 constexpr int kQBytes = 2 * kN * 128;             // 16 rows x 128 dims
 constexpr int kPBytes = 2 * kN * 128;             // P^T: 16 rows x 128 tokens
-constexpr int kThreads = 288;
 constexpr int kVProdWarp = 7;                     // issues the V boxes
 constexpr int kPvWarp = 8;                        // issues the P.V MMAs
+constexpr int kWg2Warp = 9;                       // first warp of the second softmax warpgroup
+
+// Softmax warpgroups per CTA. With 16 query columns one warpgroup's chain per
+// tile (16 maxima, the exchange, 32 exponentials, 16 stores) sets the pace, so
+// the columns are split between two warpgroups (warps 2-5 and 9-12) whose
+// chains interleave on each SM sub-partition (G = 16 on the 8B-shaped contexts:
+// 0.134 -> 0.113 ms); fewer columns keep one.
+template <int GT> struct TcCfg {
+    static constexpr int kWG = GT >= 16 ? 2 : 1;
+    static constexpr int kCols = GT / kWG;        // columns per softmax thread
+    static constexpr int kThreads = kWG == 2 ? 416 : 288;
+};
 constexpr int kMaxSeqs = 512;                     // sequences per launch (the host splits larger batches)
 constexpr uint32_t kTmemCols = 64;                // S[2] x 16 + O[2] x 16 columns
 constexpr int kPrefetchTiles = 2;                 // L2 prefetch distance, in tiles, ahead of the loads
@@ -92,9 +103,9 @@ constexpr int kBarSFree = kBarSFull + 2;                      // [2]
 constexpr int kBarPFull = kBarSFree + 2;                      // [2]
 constexpr int kBarOFull = kBarPFull + 2;                      // [2]
 constexpr int kBarOFree = kBarOFull + 2;                      // [2]
-constexpr int kBarRed = kBarOFree + 2;                        // [2]
-constexpr int kBarFin = kBarRed + 2;                          // [1]
-constexpr int kBarFullV = kBarFin + 1;                        // [kStages] V of the stage landed
+constexpr int kBarRed = kBarOFree + 2;                        // [2 warpgroups][2]
+constexpr int kBarFin = kBarRed + 4;                          // [2 warpgroups]
+constexpr int kBarFullV = kBarFin + 2;                        // [kStages] V of the stage landed
 constexpr int kNumBars = kBarFullV + kStages;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;              // tmem base, abort flag, 2 item counts
 constexpr int kOffPrefix = (kOffMisc + 32 + 15) & ~15;        // int [kMaxSeqs + 1]; later the item table
@@ -110,8 +121,9 @@ struct Bars {
     uint64_t *full, *empty;        // [kStages]
     uint64_t *s_full, *s_free;     // [2]
     uint64_t *p_full, *o_full;     // [2]
-    uint64_t *o_free, *red;        // [2]
-    uint64_t *fin;                 // [1]
+    uint64_t *o_free;              // [2]
+    uint64_t *red;                 // [warpgroup][2]
+    uint64_t *fin;                 // [warpgroup]
     uint64_t *full_v;              // [kStages]
 };
 
@@ -175,7 +187,7 @@ template <> __device__ __forceinline__ float from_bits<__half>(uint16_t b) {
 }
 
 template <typename T, int GT>
-__global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+__global__ __launch_bounds__(TcCfg<GT>::kThreads, 1) void decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                 const __grid_constant__ CUtensorMap tm_v,
                                                                 const __grid_constant__ CUtensorMap tm_q,
                                                                 const DecodeParams p) {
@@ -215,15 +227,17 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             mbar_init(&bars.full_v[s], 1);
             mbar_init(&bars.empty[s], 1);
         }
+        constexpr uint32_t kSoftWarps = 4 * TcCfg<GT>::kWG;
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
-            mbar_init(&bars.s_free[i], 4);
-            mbar_init(&bars.p_full[i], 4);
+            mbar_init(&bars.s_free[i], kSoftWarps);
+            mbar_init(&bars.p_full[i], kSoftWarps);
             mbar_init(&bars.o_full[i], 1);
-            mbar_init(&bars.o_free[i], 4);
-            mbar_init(&bars.red[i], 4);          // one arrival per softmax warp
+            mbar_init(&bars.o_free[i], kSoftWarps);
         }
-        mbar_init(bars.fin, 4);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars.red[i], 4);   // one arrival per warp of a warpgroup
+        mbar_init(&bars.fin[0], 4);
+        mbar_init(&bars.fin[1], 4);
         *abort_flag = 0;
         *loads_issued = 0;
         mbar_fence_init();
@@ -257,7 +271,8 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     const int total_items = (counts[0] + counts[1]) * p.num_kv_heads;
     // this CTA's item descriptors, computed once and kept over the ordering arrays
     int4 *items = reinterpret_cast<int4 *>(smem + kOffPrefix);
-    decode_order::build_item_table<(decode_order::kTableItems + kThreads - 1) / kThreads>(p, prefix, order, n4, cache, total_items, items);
+    constexpr int kThr = TcCfg<GT>::kThreads;
+    decode_order::build_item_table<(decode_order::kTableItems + kThr - 1) / kThr>(p, prefix, order, n4, cache, total_items, items);
     const int nmy = decode_order::cta_items(total_items);
     __syncthreads();
 
@@ -446,40 +461,52 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         }
     } else {
         // ------------------------------------------------------------ softmax / output
+        // Warpgroup wg handles query columns [c0, c0 + kC) of every tile.
+        constexpr int kC = TcCfg<GT>::kCols;
+        constexpr bool kTwo = TcCfg<GT>::kWG == 2;
+        const int wg = kTwo && warp >= kWg2Warp ? 1 : 0;
+        const int c0 = wg * kC;
         const int q4 = warp & 3;                       // tensor-memory lane quadrant
         const int row = q4 * 32 + lane;                // token (S) or dim (O) of this thread
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        uint64_t *red_bar = bars.red + 2 * wg;
+        uint64_t *fin_bar = bars.fin + wg;
         T *out = reinterpret_cast<T *>(p.out);
         uint32_t it = 0, nfin = 0;              // tile counter; uses of the finalize barrier
         bool ok = true;
-        float m_run[GT], l_part[GT], o_acc[GT], alpha_prev[GT];
+        float m_run[kC], l_part[kC], o_acc[kC], alpha_prev[kC];
+        // this warpgroup's columns of a tile's accumulator at tensor-memory column `col`
+        auto load_cols = [&](uint32_t col, float *v) {
+            if constexpr (kTwo) tmem_ld8(tmem + lane_off + col + c0, v);
+            else tmem_ld16(tmem + lane_off + col, v);
+        };
         for (int k = 0; k < nmy && ok; ++k) {
             const Item I = decode_order::unpack_item(items[k]);
             const int64_t head0 = (int64_t)I.b * p.num_heads + (int64_t)I.kvh * G;
             if (I.ntiles == 0) {
 #pragma unroll
-                for (int g = 0; g < GT; ++g)
-                    if (g < G) out[(head0 + g) * kD + row] = Elem<T>::from_f(0.f);
+                for (int u = 0; u < kC; ++u)
+                    if (c0 + u < G) out[(head0 + c0 + u) * kD + row] = Elem<T>::from_f(0.f);
                 continue;
             }
 #pragma unroll
-            for (int g = 0; g < GT; ++g) {
-                m_run[g] = -INFINITY;
-                l_part[g] = 0.f;
-                o_acc[g] = 0.f;
-                alpha_prev[g] = 0.f;
+            for (int u = 0; u < kC; ++u) {
+                m_run[u] = -INFINITY;
+                l_part[u] = 0.f;
+                o_acc[u] = 0.f;
+                alpha_prev[u] = 0.f;
             }
             auto accumulate = [&](uint32_t j) -> bool {
                 const int buf = j & 1;
                 if (!warp_wait(&bars.o_full[buf], (j >> 1) & 1)) return false;
                 tc_fence_after();
                 float o[16];
-                tmem_ld16(tmem + lane_off + 2 * kN + buf * kN, o);
+                load_cols(2 * kN + buf * kN, o);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.o_free[buf]);
 #pragma unroll
-                for (int g = 0; g < GT; ++g) o_acc[g] = fmaf(o_acc[g], alpha_prev[g], o[g]);
+                for (int u = 0; u < kC; ++u) o_acc[u] = fmaf(o_acc[u], alpha_prev[u], o[u]);
                 return true;
             };
             for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
@@ -490,7 +517,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                 }
                 tc_fence_after();
                 float s[16];
-                tmem_ld16(tmem + lane_off + buf * kN, s);
+                load_cols(buf * kN, s);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.s_free[buf]);
@@ -499,45 +526,49 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                 const bool valid = tok < I.t1;
                 float* rd = red + (it & 1) * 4 * kN;
 #pragma unroll
-                for (int g = 0; g < GT; ++g) {
-                    s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
-                    const float mx = warp_max(s[g]);
+                for (int u = 0; u < kC; ++u) {
+                    const int g = c0 + u;
+                    s[u] = valid ? s[u] * p.scale_log2 : -INFINITY;
+                    const float mx = warp_max(s[u]);
                     if (lane == 0) rd[q4 * kN + g] = mx;
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.red[it & 1]);
-                if (!warp_wait(&bars.red[it & 1], (it >> 1) & 1)) {
+                if (lane == 0) mbar_arrive(&red_bar[it & 1]);
+                if (!warp_wait(&red_bar[it & 1], (it >> 1) & 1)) {
                     ok = false;
                     break;
                 }
-                float alpha[GT];
+                float alpha[kC];
                 unsigned char *pb = sP + buf * kPBytes + (row >> 6) * (kN * 128);
                 const int colb = (row & 63) * 2;
 #pragma unroll
-                for (int g = 0; g < GT; ++g) {
+                for (int u = 0; u < kC; ++u) {
+                    const int g = c0 + u;
                     const float tmax = fmaxf(fmaxf(rd[g], rd[kN + g]), fmaxf(rd[2 * kN + g], rd[3 * kN + g]));
-                    const float m_new = fmaxf(m_run[g], tmax);
-                    alpha[g] = fast_exp2(m_run[g] - m_new);
-                    m_run[g] = m_new;
-                    const uint16_t bits = to_bits<T>(valid ? fast_exp2(s[g] - m_new) : 0.f);
-                    l_part[g] = fmaf(l_part[g], alpha[g], from_bits<T>(bits));
+                    const float m_new = fmaxf(m_run[u], tmax);
+                    alpha[u] = fast_exp2(m_run[u] - m_new);
+                    m_run[u] = m_new;
+                    const uint16_t bits = to_bits<T>(valid ? fast_exp2(s[u] - m_new) : 0.f);
+                    l_part[u] = fmaf(l_part[u], alpha[u], from_bits<T>(bits));
                     // P^T element (row n = g, column k = token) in a 128-byte swizzled K-major tile
                     unsigned char *dst = pb + g * 128 + ((((colb >> 4) ^ (g & 7)) << 4) | (colb & 15));
                     *reinterpret_cast<uint16_t *>(dst) = bits;
                 }
                 // masked token: its V row may hold anything (NaN included) and P = 0,
-                // so zero the row once the stage's copies have landed
-                if (__any_sync(0xffffffffu, !valid) && !warp_wait(&bars.full_v[stage], (it / kStages) & 1)) {
-                    ok = false;
-                    break;
-                }
-                if (!valid) {
-                    uint4 *v0 = reinterpret_cast<uint4 *>(sV + stage * kKVBytes + row * 128);
-                    uint4 *v1 = reinterpret_cast<uint4 *>(sV + stage * kKVBytes + kChunkBytes + row * 128);
+                // so zero the row once the stage's copies have landed (first warpgroup)
+                if (wg == 0) {
+                    if (__any_sync(0xffffffffu, !valid) && !warp_wait(&bars.full_v[stage], (it / kStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!valid) {
+                        uint4 *v0 = reinterpret_cast<uint4 *>(sV + stage * kKVBytes + row * 128);
+                        uint4 *v1 = reinterpret_cast<uint4 *>(sV + stage * kKVBytes + kChunkBytes + row * 128);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {           // rotated by row: no bank conflicts
-                        v0[c ^ (row & 7)] = make_uint4(0, 0, 0, 0);
-                        v1[c ^ (row & 7)] = make_uint4(0, 0, 0, 0);
+                        for (int c = 0; c < 8; ++c) {       // rotated by row: no bank conflicts
+                            v0[c ^ (row & 7)] = make_uint4(0, 0, 0, 0);
+                            v1[c ^ (row & 7)] = make_uint4(0, 0, 0, 0);
+                        }
                     }
                 }
                 fence_proxy_async_smem();
@@ -548,7 +579,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                     break;
                 }
 #pragma unroll
-                for (int g = 0; g < GT; ++g) alpha_prev[g] = alpha[g];
+                for (int u = 0; u < kC; ++u) alpha_prev[u] = alpha[u];
             }
             if (!ok) break;
             if (!accumulate(it - 1)) {
@@ -559,33 +590,36 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             // (lred is double-buffered by item parity: one barrier per item)
             float *lr = lred + (nfin & 1) * 4 * kN;
 #pragma unroll
-            for (int g = 0; g < GT; ++g) {
-                const float ls = warp_sum(l_part[g]);
-                if (lane == 0) lr[q4 * kN + g] = ls;
+            for (int u = 0; u < kC; ++u) {
+                const float ls = warp_sum(l_part[u]);
+                if (lane == 0) lr[q4 * kN + c0 + u] = ls;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.fin);
-            if (!warp_wait(bars.fin, nfin++ & 1)) {
+            if (lane == 0) mbar_arrive(fin_bar);
+            if (!warp_wait(fin_bar, nfin++ & 1)) {
                 ok = false;
                 break;
             }
-            float l_tot[GT];
+            float l_tot[kC];
 #pragma unroll
-            for (int g = 0; g < GT; ++g) l_tot[g] = lr[g] + lr[kN + g] + lr[2 * kN + g] + lr[3 * kN + g];
+            for (int u = 0; u < kC; ++u) {
+                const int g = c0 + u;
+                l_tot[u] = lr[g] + lr[kN + g] + lr[2 * kN + g] + lr[3 * kN + g];
+            }
             if (I.direct) {
 #pragma unroll
-                for (int g = 0; g < GT; ++g)
-                    if (g < G) out[(head0 + g) * kD + row] = Elem<T>::from_f(o_acc[g] / l_tot[g]);
+                for (int u = 0; u < kC; ++u)
+                    if (c0 + u < G) out[(head0 + c0 + u) * kD + row] = Elem<T>::from_f(o_acc[u] / l_tot[u]);
             } else {
                 const int P = p.max_partitions;
 #pragma unroll
-                for (int g = 0; g < GT; ++g) {
-                    if (g < G) {
-                        const int64_t r = (head0 + g) * P + I.slot;
-                        p.ws_o[r * kD + row] = o_acc[g];
+                for (int u = 0; u < kC; ++u) {
+                    if (c0 + u < G) {
+                        const int64_t r = (head0 + c0 + u) * P + I.slot;
+                        p.ws_o[r * kD + row] = o_acc[u];
                         if (row == 0) {
-                            p.ws_ml[2 * r] = m_run[g];
-                            p.ws_ml[2 * r + 1] = l_tot[g];
+                            p.ws_ml[2 * r] = m_run[u];
+                            p.ws_ml[2 * r + 1] = l_tot[u];
                         }
                     }
                 }
@@ -643,7 +677,7 @@ int launch_tc_t(const DecodeParams &p, CUtensorMapDataType dt, cudaStream_t stre
         return -1;
     const int64_t max_items = (int64_t)p.num_seqs * p.num_kv_heads * p.max_partitions;
     const int grid = (int)(max_items < num_sms[dev] ? max_items : num_sms[dev]);
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, stream, mk, mv, mq, p);
+    return launch_pdl(kern, dim3(grid), dim3(TcCfg<GT>::kThreads), kSmemBytes, stream, mk, mv, mq, p);
 }
 
 template <typename T>
