@@ -15,7 +15,7 @@
 // accumulators in tensor memory. The tensor cores take the G-fold reuse of each
 // K/V element off the FP32 pipes; the kernel stays bound by HBM.
 //
-// CTA = one persistent worker per SM; 288 threads:
+// CTA = one persistent worker per SM; 416 threads:
 //   warp 0    TMA producer of K: per tile, reads the tile's table entries (one
 //             lane per physical block, from the item's entries read once at
 //             item start) and loads each block's K rows (box = 64 dims x
@@ -35,11 +35,12 @@
 //             are in shared memory and its V has landed. Copy issue and MMA
 //             issue each cost a single thread most of a tile's time when one
 //             thread did both operands, so each operand has its own issuer.
-//   warps 2-5 softmax and output (thread = token for S, thread = dim for O):
+//   warps 2-5, 9-12  softmax and output in two warpgroups, each taking half of
+//             the query columns (thread = token for S, thread = dim for O):
 //             scale, mask, tile max through shuffles + shared memory, exp2,
 //             P^T to shared memory (bf16/f16, 128-byte swizzled K-major), zero
-//             V rows of masked tokens (their contents may be anything), and
-//             o = o * alpha + O_tile in registers.
+//             V rows of masked tokens (their contents may be anything; the first
+//             warpgroup), and o = o * alpha + O_tile in registers.
 // Work items = (sequence, partition, kv head), dealt to CTAs in serpentine
 // rounds in order of decreasing size, from a bucketed prefix sum that each CTA
 // builds in shared memory at kernel start (decode_order.cuh). Every wait is bounded (see
@@ -73,13 +74,14 @@ constexpr int kVProdWarp = 7;                     // issues the V boxes
 constexpr int kPvWarp = 8;                        // issues the P.V MMAs
 constexpr int kWg2Warp = 9;                       // first warp of the second softmax warpgroup
 
-// Softmax warpgroups per CTA. With 16 query columns one warpgroup's chain per
-// tile (16 maxima, the exchange, 32 exponentials, 16 stores) sets the pace, so
-// the columns are split between two warpgroups (warps 2-5 and 9-12) whose
-// chains interleave on each SM sub-partition (G = 16 on the 8B-shaped contexts:
-// 0.134 -> 0.113 ms); fewer columns keep one.
+// Softmax warpgroups per CTA. One warpgroup's chain per tile (the column maxima,
+// the exchange, two exponentials and a store per column, the O accumulation)
+// set the pace at 16 query columns, so the columns are split between two
+// warpgroups (warps 2-5 and 9-12) whose chains interleave on each SM
+// sub-partition: G = 16 on the 8B-shaped contexts 0.134 -> 0.112 ms; G = 8 (long
+// context) 0.4040 -> 0.3998 ms; G = 4 0.0998 -> 0.0995 ms.
 template <int GT> struct TcCfg {
-    static constexpr int kWG = GT >= 16 ? 2 : 1;
+    static constexpr int kWG = 2;
     static constexpr int kCols = GT / kWG;        // columns per softmax thread
     static constexpr int kThreads = kWG == 2 ? 416 : 288;
 };
