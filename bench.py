@@ -58,7 +58,7 @@ def hbm_peak():
 _KERNEL_SOURCES = {
     "decode_tc": ["decode_tc.cu", "decode_order.cuh", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
     "decode_fp8": ["decode_fp8.cu", "decode_order.cuh", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h",
-                   "kernels_fp8.h"],
+                   "kernels_fp8.h", "fp8_encode.cuh"],
     "prefill_tc": ["prefill_tc.cu", "prefill_common.cuh", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
 }
 
@@ -279,7 +279,7 @@ class Step:
         # a step whose new tokens are the batch's own newest ones (not mixed serving's
         # extra write, not the 8-bit or shared paths) runs as one decode-with-append
         # call: the tensor-core decode writes each token before reading its block
-        self.append = not self.fp8 and self.shared is None and not name.startswith("mixed_serving")
+        self.append = self.shared is None and not name.startswith("mixed_serving")
         self.launches_per_step = (0 if self.append else 1) + (1 if self.copy_pairs is not None else 0) + 1 + (
             1 if pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, self.max_ctx, 0) else 0)
         if self.shared is not None:
@@ -322,7 +322,12 @@ class Step:
     def decode(self, q, bt, cl, prefix=None, new=None):
         """The decode call; new = (k, v, slots) of the step's tokens for a decode with append."""
         pa = self.pa
-        if new is not None:
+        if new is not None and self.fp8:
+            k, v, slots = new
+            pa.paged_attention_decode_fp8_append(self.out, q, k, v, slots, self.kc, self.vc, bt, cl, self.w.scale,
+                                                 self.k_scale, self.v_scale, max_context_len=self.max_ctx,
+                                                 workspace=self.ws)
+        elif new is not None:
             k, v, slots = new
             pa.paged_attention_decode_append(self.out, q, k, v, slots, self.kc, self.vc, bt, cl, self.w.scale,
                                              max_context_len=self.max_ctx, workspace=self.ws)
@@ -801,7 +806,8 @@ def decode_roofline(torch, st: "Step", device, peak: float, peak_kind: str, ms_s
     achieved = bytes_ / (kern_ms * 1e-3) / 1e9
     ref_ms = ms_step if ms_step is not None else kern_ms
     frac, why = checked_roofline(achieved, peak, kern_ms, ref_ms)
-    kernel = ("decode_fp8_kernel + merge" if st.fp8 else
+    kernel = (("decode call: decode_fp8_kernel (partitions; writes the new tokens) + merge" if st.append
+               else "decode_fp8_kernel + merge") if st.fp8 else
               "shared-prefix pass + private decode_tc_kernel pass + merge" if shared else
               "decode call: decode_tc_kernel (partitions; writes the new tokens) + merge")
     roof = {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peak,

@@ -345,6 +345,32 @@ int pa_paged_attention_decode_fp8(void *out, const void *q, const void *key_cach
                                   size_t workspace_bytes, int dtype, void *stream);
 
 /*
+ * One decode step over E4M3 caches: pa_paged_kv_write_fp8 of each sequence's new
+ * token, then pa_paged_attention_decode_fp8. [P2 demo 1: a decode step writes
+ * the new token's KV into its slot, then attends over the whole context, that
+ * token included; P3 B.2: slot_mapping]
+ *
+ * k_new, v_new: [num_seqs, num_kv_heads, head_dim] in dtype (the query's bf16 or
+ * f16, 16-byte aligned), the new token of sequence b in row b; slot_mapping[b]:
+ * its slot, which must be the slot of position context_lens[b] - 1, or -1 for
+ * no write (the only value allowed for an empty context). The decode kernel
+ * quantises and stores each token itself, with the scatter's encoding (the
+ * nearest code of x / k_scale or x / v_scale), just before it reads the token's
+ * block; a slot other than that of position ctx - 1 sets PA_DEVERR_SLOT and is
+ * not written. The block holding a sequence's new token must not be read by
+ * another sequence of the same call (copy-on-write guarantees it). The result,
+ * the caches and the other arguments are those of pa_paged_kv_write_fp8
+ * followed by pa_paged_attention_decode_fp8.
+ */
+int pa_paged_attention_decode_fp8_append(void *out, const void *q, const void *k_new, const void *v_new,
+                                         const int32_t *slot_mapping, void *key_cache, void *value_cache,
+                                         const int32_t *block_tables, int max_blocks_per_seq,
+                                         const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int64_t num_blocks, float scale,
+                                         float k_scale, float v_scale, int max_context_len, int partition_size,
+                                         void *workspace, size_t workspace_bytes, int dtype, void *stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's error word.
  * *bits receives the PA_DEVERR_* bits seen since the last call. Returns
  * PA_ERR_DEVICE_INDEX when any bit was set, PA_OK otherwise.

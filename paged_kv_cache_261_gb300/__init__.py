@@ -89,6 +89,8 @@ _decl("pa_prefix_groups", [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, cty
 _decl("pa_paged_kv_write_fp8", [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _f, _f, _i32, _vp])
 _decl("pa_paged_attention_decode_fp8", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                         _i64, _f, _f, _f, _i32, _i32, _vp, _sz, _i32, _vp])
+_decl("pa_paged_attention_decode_fp8_append", [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
+                                               _i32, _i32, _i32, _i64, _f, _f, _f, _i32, _i32, _vp, _sz, _i32, _vp])
 _decl("pa_paged_attention_prefill", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
                                      _i32, _i64, _f, _i32, _vp])
 
@@ -472,6 +474,50 @@ def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, con
                                             float(k_scale), float(v_scale), int(max_context_len),
                                             int(partition_size), ws_ptr, ws_bytes, _dtype_code(q), sp)
     _check(rc, "pa_paged_attention_decode_fp8")
+
+
+def paged_attention_decode_fp8_append(out, q, k_new, v_new, slot_mapping, key_cache, value_cache, block_tables,
+                                      context_lens, scale: float, k_scale: float, v_scale: float,
+                                      max_context_len: int = 0, partition_size: int = 0, workspace=None,
+                                      stream=None) -> None:
+    """One decode step over 8-bit caches: each sequence's new token (k_new, v_new
+    [B, Hk, D] in q's dtype) is quantised into slot_mapping[b] -- the slot of
+    position context_lens[b] - 1, or -1 -- by the decode kernel itself, then the
+    decode runs. The same result and caches as paged_kv_write_fp8 followed by
+    paged_attention_decode_fp8."""
+    torch = _torch()
+    dev = key_cache.device
+    nb, bs, hk, d = _fp8_caches(key_cache, value_cache, dev)
+    _cuda(q, "q", None, dev)
+    _cuda(out, "out", q.dtype, dev)
+    _cuda(k_new, "k_new", q.dtype, dev)
+    _cuda(v_new, "v_new", q.dtype, dev)
+    _cuda(slot_mapping, "slot_mapping", torch.int32, dev)
+    _cuda(block_tables, "block_tables", torch.int32, dev)
+    _cuda(context_lens, "context_lens", torch.int32, dev)
+    B, H, D = q.shape
+    if D != d or tuple(out.shape) != (B, H, D):
+        raise ValueError("q/out must be [B, H, head_dim]")
+    if tuple(k_new.shape) != (B, hk, D) or tuple(v_new.shape) != (B, hk, D) or tuple(slot_mapping.shape) != (B,):
+        raise ValueError("k_new/v_new must be [B, num_kv_heads, head_dim] and slot_mapping [B]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_tables must be [B, MB] and context_lens [B]")
+    mb = block_tables.shape[1]
+    sp = _stream_ptr(stream, dev)
+    need = decode_workspace_bytes(B, H, D, max_context_len or mb * bs, partition_size)
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            workspace = _workspace(dev, sp, need)
+        _cuda(workspace, "workspace", torch.uint8, dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    rc = _lib.pa_paged_attention_decode_fp8_append(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                                   slot_mapping.data_ptr(), key_cache.data_ptr(),
+                                                   value_cache.data_ptr(), block_tables.data_ptr(), mb,
+                                                   context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
+                                                   float(k_scale), float(v_scale), int(max_context_len),
+                                                   int(partition_size), ws_ptr, ws_bytes, _dtype_code(q), sp)
+    _check(rc, "pa_paged_attention_decode_fp8_append")
 
 
 def get_device_error(stream=None, device=None) -> int:

@@ -154,6 +154,40 @@ int decode_workspace(pa::DecodeParams &p, int64_t P, void *workspace, size_t wor
     return PA_OK;
 }
 
+// The 8-bit decode, optionally with append (k_new, v_new and slot_mapping non-NULL:
+// the kernel quantises and stores each sequence's new K/V row itself).
+int decode_fp8_call(void *out, const void *q, const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                    const void *key_cache, const void *value_cache, const int32_t *block_tables,
+                    int max_blocks_per_seq, const int32_t *context_lens, int num_seqs, int num_heads,
+                    int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, float scale, float k_scale,
+                    float v_scale, int max_context_len, int partition_size, void *workspace, size_t workspace_bytes,
+                    int dtype, void *stream) {
+    if (dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F16) return elem_size(dtype) ? PA_ERR_UNSUPPORTED
+                                                                                  : PA_ERR_INVALID_ARG;
+    if (!finite_positive(k_scale) || !finite_positive(v_scale)) return PA_ERR_INVALID_ARG;
+    pa::DecodeParams p{};
+    int64_t P = 0;
+    int rc = decode_setup(p, P, out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                          num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                          max_context_len, partition_size);
+    if (rc == kNothingToDo) return PA_OK;
+    if (rc != PA_OK) return rc;
+    if (!pa::decode_fp8_supported(p, dtype)) return PA_ERR_UNSUPPORTED;
+    if ((rc = error_word(&p.err)) != PA_OK) return rc;
+    p.scale_log2 = scale * k_scale * pa::kLog2e;                  // k_scale folded into the score scale
+    p.app_k = k_new;
+    p.app_v = v_new;
+    p.app_slots = slot_mapping;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *owned = nullptr;
+    if ((rc = decode_workspace(p, P, workspace, workspace_bytes, s, &owned)) != PA_OK) return rc;
+    int krc = pa::launch_decode_fp8(p, v_scale, k_scale, dtype, s);
+    if (krc == 0 && P > 1) krc = pa::launch_decode_reduce(p, dtype, s);
+    if (owned) cudaFreeAsync(owned, s);
+    if (krc == -2) return PA_ERR_UNSUPPORTED;
+    return krc == 0 ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -321,27 +355,25 @@ int pa_paged_attention_decode_fp8(void *out, const void *q, const void *key_cach
                                   float v_scale, int max_context_len, int partition_size, void *workspace,
                                   size_t workspace_bytes, int dtype, void *stream) {
     const pa::CallRange range(__func__);
-    if (dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F16) return elem_size(dtype) ? PA_ERR_UNSUPPORTED
-                                                                                  : PA_ERR_INVALID_ARG;
-    if (!finite_positive(k_scale) || !finite_positive(v_scale)) return PA_ERR_INVALID_ARG;
-    pa::DecodeParams p{};
-    int64_t P = 0;
-    int rc = decode_setup(p, P, out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
-                          num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                          max_context_len, partition_size);
-    if (rc == kNothingToDo) return PA_OK;
-    if (rc != PA_OK) return rc;
-    if (!pa::decode_fp8_supported(p, dtype)) return PA_ERR_UNSUPPORTED;
-    if ((rc = error_word(&p.err)) != PA_OK) return rc;
-    p.scale_log2 = scale * k_scale * pa::kLog2e;                  // k_scale folded into the score scale
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    void *owned = nullptr;
-    if ((rc = decode_workspace(p, P, workspace, workspace_bytes, s, &owned)) != PA_OK) return rc;
-    int krc = pa::launch_decode_fp8(p, v_scale, dtype, s);
-    if (krc == 0 && P > 1) krc = pa::launch_decode_reduce(p, dtype, s);
-    if (owned) cudaFreeAsync(owned, s);
-    if (krc == -2) return PA_ERR_UNSUPPORTED;
-    return krc == 0 ? PA_OK : PA_ERR_CUDA;
+    return decode_fp8_call(out, q, nullptr, nullptr, nullptr, key_cache, value_cache, block_tables,
+                           max_blocks_per_seq, context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                           num_blocks, scale, k_scale, v_scale, max_context_len, partition_size, workspace,
+                           workspace_bytes, dtype, stream);
+}
+
+int pa_paged_attention_decode_fp8_append(void *out, const void *q, const void *k_new, const void *v_new,
+                                         const int32_t *slot_mapping, void *key_cache, void *value_cache,
+                                         const int32_t *block_tables, int max_blocks_per_seq,
+                                         const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int64_t num_blocks, float scale,
+                                         float k_scale, float v_scale, int max_context_len, int partition_size,
+                                         void *workspace, size_t workspace_bytes, int dtype, void *stream) {
+    const pa::CallRange range(__func__);
+    if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_INVALID_ARG;
+    return decode_fp8_call(out, q, k_new, v_new, slot_mapping, key_cache, value_cache, block_tables,
+                           max_blocks_per_seq, context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                           num_blocks, scale, k_scale, v_scale, max_context_len, partition_size, workspace,
+                           workspace_bytes, dtype, stream);
 }
 
 size_t pa_decode_shared_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,

@@ -53,6 +53,7 @@
 
 #include "common.cuh"
 #include "decode_order.cuh"
+#include "fp8_encode.cuh"
 #include "kernels.h"
 #include "kernels_fp8.h"
 #include "sm100.cuh"
@@ -235,10 +236,47 @@ template <> __device__ __forceinline__ void unpack4<__half>(uint2 u, float *x) {
     x[3] = b.y;
 }
 
-template <typename T, int GT>
+// Decode with append (kApp): the step's own token of the item's sequence (position
+// ctx - 1), for the item's kv head. At the start of the sequence's last item, before
+// any of its tiles is loaded, the producer warps read its slot, encode their row (K
+// with k_scale by the K producer, V with v_scale by the V producer: lanes 0-7 each
+// 16 elements, the scatter's encoding) and store the codes, so the item's TMA loads
+// read them. (Storing just before the last tile's loads instead, with a check on
+// every tile, measured slower: long context 0.2368 against 0.2346 ms a step.) `e`
+// is the block-table entry of the token's block. The slot must be that of position
+// ctx - 1 (a different one sets PA_DEVERR_SLOT and is not written; -1 writes
+// nothing).
+template <typename T>
+__device__ __forceinline__ uint4 append_codes(const DecodeParams &p, const Item &I, bool is_v, float scale,
+                                              int lane) {
+    if (lane >= kD / 16) return make_uint4(0, 0, 0, 0);
+    const T *src = static_cast<const T *>(is_v ? p.app_v : p.app_k) +
+                   ((int64_t)I.b * p.num_kv_heads + I.kvh) * kD + lane * 16;
+    float x[16];
+    fp8::load16(src, x);
+    return fp8::encode16(x, scale);
+}
+
+__device__ __forceinline__ void append_store(const DecodeParams &p, const Item &I, int slot, int e, uint4 codes,
+                                             bool is_v, int lane) {
+    const int pos = I.t1 - 1;
+    const int64_t expect = (int64_t)e * p.block_size + (pos & (p.block_size - 1));
+    if (e < 0 || e >= p.num_blocks || (int64_t)slot != expect) {
+        if (!is_v && lane == 0) raise_error(p.err, PA_DEVERR_SLOT);
+        return;
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<unsigned char *>(
+                     const_cast<void *>(is_v ? p.value_cache : p.key_cache)) +
+                     ((int64_t)slot * p.num_kv_heads + I.kvh) * kD);
+    if (lane < kD / 16) dst[lane] = codes;
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // the tile's TMA loads read them
+}
+
+template <typename T, int GT, bool kApp>
 __global__ __launch_bounds__(kThreads, ctas_per_sm(GT)) void decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
-                                                                 const DecodeParams p, const float v_scale) {
+                                                                 const DecodeParams p, const float v_scale,
+                                                                 const float k_scale) {
     constexpr int NT = n_cols(GT);
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -349,6 +387,24 @@ __global__ __launch_bounds__(kThreads, ctas_per_sm(GT)) void decode_fp8_kernel(c
         for (int k = 0; k < nmy && ok; ++k) {
             const Item I = decode_order::unpack_item(items[k]);
             const decode_order::ItemTable tb = decode_order::load_item_table(p, I, lane);
+            // decode with append: the new token's slot and codes, used at the item's
+            // last tile (an empty context takes only -1)
+            if constexpr (kApp) {
+                if (I.last) {
+                    const int app_slot = p.app_slots[I.b];
+                    if (app_slot != -1 && I.ntiles > 0) {
+                        const uint4 app_codes = append_codes<T>(p, I, is_v, is_v ? v_scale : k_scale, lane);
+                        // the token's block among the item's blocks, from the table in registers
+                        const int jb = ((I.t1 - 1) >> p.log2_block_size) - (I.t0 >> p.log2_block_size);
+                        bool lv;
+                        const int e = decode_order::tile_entry(tb, jb / nbt, nbt, lane, &lv);
+                        append_store(p, I, app_slot, __shfl_sync(0xffffffffu, e, jb % nbt), app_codes, is_v, lane);
+                        __syncwarp();
+                    }
+                    if (app_slot != -1 && I.ntiles == 0 && I.t1 == 0 && !is_v && lane == 0)
+                        raise_error(p.err, PA_DEVERR_SLOT);
+                }
+            }
             for (int tile = 0; tile < I.ntiles; ++tile, ++it) {
                 const int stage = it % nstages;
                 const uint32_t ph = (it / nstages) & 1;
@@ -779,9 +835,9 @@ bool make_cache_map_u8(CUtensorMap *m, const void *base, const DecodeParams &p) 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int GT>
-int launch_t(const DecodeParams &p, float v_scale, cudaStream_t stream) {
-    auto kern = decode_fp8_kernel<T, GT>;
+template <typename T, int GT, bool kApp>
+int launch_t(const DecodeParams &p, float v_scale, float k_scale, cudaStream_t stream) {
+    auto kern = decode_fp8_kernel<T, GT, kApp>;
     static bool attr_set[kMaxDevices] = {};
     static int num_sms[kMaxDevices] = {};
     int dev = 0;
@@ -797,14 +853,19 @@ int launch_t(const DecodeParams &p, float v_scale, cudaStream_t stream) {
     const int64_t max_items = (int64_t)p.num_seqs * p.num_kv_heads * p.max_partitions;
     const int64_t slots = (int64_t)ctas_per_sm(GT) * num_sms[dev];
     const int grid = (int)(max_items < slots ? max_items : slots);
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, stream, mk, mv, p, v_scale);
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, stream, mk, mv, p, v_scale, k_scale);
+}
+
+template <typename T, bool kApp>
+int launch_g(const DecodeParams &p, float v_scale, float k_scale, cudaStream_t stream) {
+    if (p.group <= 4) return launch_t<T, 4, kApp>(p, v_scale, k_scale, stream);
+    if (p.group <= 8) return launch_t<T, 8, kApp>(p, v_scale, k_scale, stream);
+    return launch_t<T, 16, kApp>(p, v_scale, k_scale, stream);
 }
 
 template <typename T>
-int launch_g(const DecodeParams &p, float v_scale, cudaStream_t stream) {
-    if (p.group <= 4) return launch_t<T, 4>(p, v_scale, stream);
-    if (p.group <= 8) return launch_t<T, 8>(p, v_scale, stream);
-    return launch_t<T, 16>(p, v_scale, stream);
+int launch_a(const DecodeParams &p, float v_scale, float k_scale, cudaStream_t stream) {
+    return p.app_slots ? launch_g<T, true>(p, v_scale, k_scale, stream) : launch_g<T, false>(p, v_scale, k_scale, stream);
 }
 
 }  // namespace
@@ -816,7 +877,7 @@ bool decode_fp8_supported(const DecodeParams &p, int dtype) {
 }
 
 // Batches above kMaxSeqs sequences run as independent launches of up to kMaxSeqs.
-int launch_decode_fp8(const DecodeParams &p, float v_scale, int dtype, cudaStream_t stream) {
+int launch_decode_fp8(const DecodeParams &p, float v_scale, float k_scale, int dtype, cudaStream_t stream) {
     if (!decode_fp8_supported(p, dtype)) return -2;
     // sequences per launch: at most kMaxSeqs, and few enough that no CTA gets more
     // than the item table holds (items <= num_seqs * kv heads * partitions)
@@ -841,8 +902,13 @@ int launch_decode_fp8(const DecodeParams &p, float v_scale, int dtype, cudaStrea
             c.ws_ml = p.ws_ml + rows * p.max_partitions * 2;
             c.ws_o = p.ws_o + rows * p.max_partitions * kD;
         }
-        const int rc = dtype == PA_DTYPE_BF16 ? launch_g<__nv_bfloat16>(c, v_scale, stream)
-                                              : launch_g<__half>(c, v_scale, stream);
+        if (p.app_slots) {
+            c.app_slots = p.app_slots + b0;
+            c.app_k = static_cast<const char *>(p.app_k) + (int64_t)b0 * p.num_kv_heads * kD * 2;
+            c.app_v = static_cast<const char *>(p.app_v) + (int64_t)b0 * p.num_kv_heads * kD * 2;
+        }
+        const int rc = dtype == PA_DTYPE_BF16 ? launch_a<__nv_bfloat16>(c, v_scale, k_scale, stream)
+                                              : launch_a<__half>(c, v_scale, k_scale, stream);
         if (rc != 0) return rc;
     }
     return 0;

@@ -72,19 +72,15 @@ constexpr int kQBytes = 2 * kN * 128;             // 16 rows x 128 dims
 constexpr int kPBytes = 2 * kN * 128;             // P^T: 16 rows x 128 tokens
 constexpr int kVProdWarp = 7;                     // issues the V boxes
 constexpr int kPvWarp = 8;                        // issues the P.V MMAs
-constexpr int kWg2Warp = 9;                       // first warp of the second softmax warpgroup
 
-// Softmax warpgroups per CTA. One warpgroup's chain per tile (the column maxima,
-// the exchange, two exponentials and a store per column, the O accumulation)
-// set the pace at 16 query columns, so the columns are split between two
-// warpgroups (warps 2-5 and 9-12) whose chains interleave on each SM
+// Two softmax warpgroups per CTA (warps 2-5 and 9-12), each taking half of the
+// padded query columns of every tile. One warpgroup's chain per tile (the column
+// maxima, the exchange, two exponentials and a store per column, the O
+// accumulation) set the pace at 16 query columns; two interleave on each SM
 // sub-partition: G = 16 on the 8B-shaped contexts 0.134 -> 0.112 ms; G = 8 (long
 // context) 0.4040 -> 0.3998 ms; G = 4 0.0998 -> 0.0995 ms.
-template <int GT> struct TcCfg {
-    static constexpr int kWG = 2;
-    static constexpr int kCols = GT / kWG;        // columns per softmax thread
-    static constexpr int kThreads = kWG == 2 ? 416 : 288;
-};
+constexpr int kThreads = 416;
+constexpr int kWg2Warp = 9;                       // first warp of the second softmax warpgroup
 constexpr int kMaxSeqs = 512;                     // sequences per launch (the host splits larger batches)
 constexpr uint32_t kTmemCols = 64;                // S[2] x 16 + O[2] x 16 columns
 constexpr int kPrefetchTiles = 2;                 // L2 prefetch distance, in tiles, ahead of the loads
@@ -189,7 +185,7 @@ template <> __device__ __forceinline__ float from_bits<__half>(uint16_t b) {
 }
 
 template <typename T, int GT>
-__global__ __launch_bounds__(TcCfg<GT>::kThreads, 1) void decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+__global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                 const __grid_constant__ CUtensorMap tm_v,
                                                                 const __grid_constant__ CUtensorMap tm_q,
                                                                 const DecodeParams p) {
@@ -229,7 +225,7 @@ __global__ __launch_bounds__(TcCfg<GT>::kThreads, 1) void decode_tc_kernel(const
             mbar_init(&bars.full_v[s], 1);
             mbar_init(&bars.empty[s], 1);
         }
-        constexpr uint32_t kSoftWarps = 4 * TcCfg<GT>::kWG;
+        constexpr uint32_t kSoftWarps = 8;                     // two warpgroups
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
             mbar_init(&bars.s_free[i], kSoftWarps);
@@ -273,8 +269,7 @@ __global__ __launch_bounds__(TcCfg<GT>::kThreads, 1) void decode_tc_kernel(const
     const int total_items = (counts[0] + counts[1]) * p.num_kv_heads;
     // this CTA's item descriptors, computed once and kept over the ordering arrays
     int4 *items = reinterpret_cast<int4 *>(smem + kOffPrefix);
-    constexpr int kThr = TcCfg<GT>::kThreads;
-    decode_order::build_item_table<(decode_order::kTableItems + kThr - 1) / kThr>(p, prefix, order, n4, cache, total_items, items);
+    decode_order::build_item_table<(decode_order::kTableItems + kThreads - 1) / kThreads>(p, prefix, order, n4, cache, total_items, items);
     const int nmy = decode_order::cta_items(total_items);
     __syncthreads();
 
@@ -464,9 +459,8 @@ __global__ __launch_bounds__(TcCfg<GT>::kThreads, 1) void decode_tc_kernel(const
     } else {
         // ------------------------------------------------------------ softmax / output
         // Warpgroup wg handles query columns [c0, c0 + kC) of every tile.
-        constexpr int kC = TcCfg<GT>::kCols;
-        constexpr bool kTwo = TcCfg<GT>::kWG == 2;
-        const int wg = kTwo && warp >= kWg2Warp ? 1 : 0;
+        constexpr int kC = GT / 2;
+        const int wg = warp >= kWg2Warp ? 1 : 0;
         const int c0 = wg * kC;
         const int q4 = warp & 3;                       // tensor-memory lane quadrant
         const int row = q4 * 32 + lane;                // token (S) or dim (O) of this thread
@@ -478,10 +472,8 @@ __global__ __launch_bounds__(TcCfg<GT>::kThreads, 1) void decode_tc_kernel(const
         bool ok = true;
         float m_run[kC], l_part[kC], o_acc[kC], alpha_prev[kC];
         // this warpgroup's columns of a tile's accumulator at tensor-memory column `col`
-        auto load_cols = [&](uint32_t col, float *v) {
-            if constexpr (kTwo) tmem_ld8(tmem + lane_off + col + c0, v);
-            else tmem_ld16(tmem + lane_off + col, v);
-        };
+        // (8 columns loaded; the first kC are this warpgroup's)
+        auto load_cols = [&](uint32_t col, float *v) { tmem_ld8(tmem + lane_off + col + c0, v); };
         for (int k = 0; k < nmy && ok; ++k) {
             const Item I = decode_order::unpack_item(items[k]);
             const int64_t head0 = (int64_t)I.b * p.num_heads + (int64_t)I.kvh * G;
@@ -502,7 +494,7 @@ __global__ __launch_bounds__(TcCfg<GT>::kThreads, 1) void decode_tc_kernel(const
                 const int buf = j & 1;
                 if (!warp_wait(&bars.o_full[buf], (j >> 1) & 1)) return false;
                 tc_fence_after();
-                float o[16];
+                float o[8];
                 load_cols(2 * kN + buf * kN, o);
                 tc_fence_before();
                 __syncwarp();
@@ -518,7 +510,7 @@ __global__ __launch_bounds__(TcCfg<GT>::kThreads, 1) void decode_tc_kernel(const
                     break;
                 }
                 tc_fence_after();
-                float s[16];
+                float s[8];
                 load_cols(buf * kN, s);
                 tc_fence_before();
                 __syncwarp();
@@ -679,7 +671,7 @@ int launch_tc_t(const DecodeParams &p, CUtensorMapDataType dt, cudaStream_t stre
         return -1;
     const int64_t max_items = (int64_t)p.num_seqs * p.num_kv_heads * p.max_partitions;
     const int grid = (int)(max_items < num_sms[dev] ? max_items : num_sms[dev]);
-    return launch_pdl(kern, dim3(grid), dim3(TcCfg<GT>::kThreads), kSmemBytes, stream, mk, mv, mq, p);
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, stream, mk, mv, mq, p);
 }
 
 template <typename T>

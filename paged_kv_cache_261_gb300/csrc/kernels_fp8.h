@@ -21,8 +21,11 @@ int launch_kv_write_fp8(const void *k, const void *v, int src_dtype, const int32
 // Tensor-core decode over E4M3 caches (query/output bf16 or f16, head_dim 128,
 // group <= 16, block size 8..128). p.scale_log2 must already include k_scale;
 // v_scale multiplies the output. Partials for multi-partition sequences go to
-// p.ws_ml / p.ws_o for launch_decode_reduce.
+// p.ws_ml / p.ws_o for launch_decode_reduce. With p.app_slots set (decode with
+// append) the kernel also quantises and stores each sequence's new K/V row
+// (p.app_k / p.app_v, in the query dtype) with k_scale / v_scale, as
+// launch_kv_write_fp8 would, before it reads that row's block.
 bool decode_fp8_supported(const DecodeParams &p, int dtype);
-int launch_decode_fp8(const DecodeParams &p, float v_scale, int dtype, cudaStream_t stream);
+int launch_decode_fp8(const DecodeParams &p, float v_scale, float k_scale, int dtype, cudaStream_t stream);
 
 }  // namespace pa

@@ -10,6 +10,7 @@
 // of one token's K or V row: it turns 16 source elements into one 16-byte run
 // of codes, so even a batch of a few tokens spreads its divisions over the GPU.
 #include "common.cuh"
+#include "fp8_encode.cuh"
 #include "kernels_fp8.h"
 
 namespace pa {
@@ -17,32 +18,8 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// 16 consecutive source elements (16-byte aligned) as floats.
-template <typename TS>
-__device__ __forceinline__ void load16(const TS *src, float *f) {
-    constexpr int kPer = Vec16<TS>::N;                 // elements per 16-byte vector
-#pragma unroll
-    for (int u = 0; u < 16 / kPer; ++u) {
-        const uint4 w = __ldcs(reinterpret_cast<const uint4 *>(src) + u);
-        Vec16<TS>::unpack(w, f + u * kPer);
-    }
-}
-
-// Codes of x[0..15] / scale, code i in byte i of the result.
-__device__ __forceinline__ uint4 encode16(const float *x, float scale) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint16_t lo, hi;
-        const float a = __fdiv_rn(x[4 * i], scale), b = __fdiv_rn(x[4 * i + 1], scale);
-        const float c = __fdiv_rn(x[4 * i + 2], scale), d = __fdiv_rn(x[4 * i + 3], scale);
-        // the first source operand lands in the upper byte
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
-        w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
+using fp8::encode16;
+using fp8::load16;
 
 template <typename TS>
 __global__ __launch_bounds__(kThreads) void kv_write_fp8_kernel(

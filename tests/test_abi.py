@@ -29,6 +29,7 @@ def test_header_declares_the_boundary_calls():
     names = _declared_functions()
     for must in ("pa_paged_kv_write", "pa_paged_attention_decode", "pa_copy_blocks",
                  "pa_paged_kv_write_fp8", "pa_paged_attention_decode_fp8",
+                 "pa_paged_attention_decode_fp8_append", "pa_paged_attention_decode_append",
                  "pa_decode_workspace_bytes", "pa_get_device_error", "pa_alloc_create",
                  "pa_alloc_append", "pa_alloc_fork", "pa_alloc_free_seq"):
         assert must in names
