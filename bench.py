@@ -249,8 +249,11 @@ class Step:
         self.bt = torch.as_tensor(w.block_tables, device=device)
         self.cl = torch.as_tensor(w.context_lens, device=device)
         self.max_ctx = int(w.context_lens.max())
+        # the long-context configuration names its split-K partition (512 tokens); the
+        # others leave it to the library's automatic choice
+        self.part = 512 if name.startswith("long_context") else 0
         self.ws = torch.empty(max(pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim,
-                                                            self.max_ctx, 0), 16),
+                                                            self.max_ctx, self.part), 16),
                               dtype=torch.uint8, device=device)
         self.shared = None
         self.unique_kv_bytes = None
@@ -281,7 +284,7 @@ class Step:
         # call: the tensor-core decode writes each token before reading its block
         self.append = self.shared is None and not name.startswith("mixed_serving")
         self.launches_per_step = (0 if self.append else 1) + (1 if self.copy_pairs is not None else 0) + 1 + (
-            1 if pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, self.max_ctx, 0) else 0)
+            1 if pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, self.max_ctx, self.part) else 0)
         if self.shared is not None:
             self.launches_per_step = 1 + 1 + 3     # copy, write, shared pass + private pass + merge
         torch.cuda.synchronize()
@@ -326,21 +329,23 @@ class Step:
             k, v, slots = new
             pa.paged_attention_decode_fp8_append(self.out, q, k, v, slots, self.kc, self.vc, bt, cl, self.w.scale,
                                                  self.k_scale, self.v_scale, max_context_len=self.max_ctx,
-                                                 workspace=self.ws)
+                                                 partition_size=self.part, workspace=self.ws)
         elif new is not None:
             k, v, slots = new
             pa.paged_attention_decode_append(self.out, q, k, v, slots, self.kc, self.vc, bt, cl, self.w.scale,
-                                             max_context_len=self.max_ctx, workspace=self.ws)
+                                             max_context_len=self.max_ctx, partition_size=self.part,
+                                             workspace=self.ws)
         elif self.shared is not None:
             pl, gm, mp = self.shared if prefix is None else prefix
             pa.paged_attention_decode_shared(self.out, q, self.kc, self.vc, bt, cl, pl, gm, self.w.scale,
                                              max_context_len=self.max_ctx, max_prefix_len=mp, workspace=self.ws)
         elif self.fp8:
             pa.paged_attention_decode_fp8(self.out, q, self.kc, self.vc, bt, cl, self.w.scale, self.k_scale,
-                                          self.v_scale, max_context_len=self.max_ctx, workspace=self.ws)
+                                          self.v_scale, max_context_len=self.max_ctx, partition_size=self.part,
+                                          workspace=self.ws)
         else:
             pa.paged_attention_decode(self.out, q, self.kc, self.vc, bt, cl, self.w.scale,
-                                      max_context_len=self.max_ctx, workspace=self.ws)
+                                      max_context_len=self.max_ctx, partition_size=self.part, workspace=self.ws)
 
     def decode_call(self):
         """The step's decode call alone (with its write when it is a decode with append)."""
@@ -364,7 +369,8 @@ class Step:
                 "write": ("fused: decode with append (each sequence's new token written by the decode kernel)"
                           if self.append else "separate scatter launch"),
                 "copied_blocks": 0 if self.copy_pairs is None else int(self.copy_pairs.shape[0]),
-                "partition_size": 512,
+                "partition_size": (512 if self.shared is not None else
+                                   self.pa.decode_partition_size(w.num_seqs, self.max_ctx, self.part)),
                 "shared_prefix_decode": self.shared is not None,
                 "unique_kv_bytes": self.unique_kv_bytes,
                 "kv_cache": (f"e4m3 codes, k_scale = v_scale = {self.k_scale:.9g}" if self.fp8 else w.dtype),

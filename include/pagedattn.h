@@ -103,6 +103,17 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                  int max_context_len, int partition_size);
 
 /*
+ * The partition size a decode call uses for these arguments: partition_size
+ * itself when it is not 0, else the automatic choice -- 1024 tokens when
+ * num_seqs * ceil(max_context_len / 1024) >= 64, otherwise 512 (small batches
+ * keep more, shorter partitions to spread over the SMs). max_context_len is the
+ * call's bound (max_blocks_per_seq * block_size when the call passes 0).
+ * Applies to pa_paged_attention_decode, _append, _noalloc and the _fp8 calls;
+ * the sharing-aware decode uses 512 when given 0.
+ */
+int pa_decode_partition_size(int num_seqs, int max_context_len, int partition_size);
+
+/*
  * Single-query decode attention over the paged cache.
  * [P2 demo 2, eq. 4: for each sequence and query head, scores against every
  *  cached key are formed block by block through the block table, ONE softmax
@@ -116,7 +127,8 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
  * fp32; out has q's dtype. context_lens[b] == 0 gives a zero row.
  *
  * Long contexts are split into partitions of partition_size tokens
- * (0 = automatic, else a positive multiple of 128). Each partition keeps its
+ * (0 = automatic, see pa_decode_partition_size; else a positive multiple of
+ * 128). Each partition keeps its
  * running max, sum and unnormalised output in fp32 workspace, and a second
  * kernel merges them. max_context_len is a host-side upper bound on every
  * context_lens[b] (0 = max_blocks_per_seq * block_size); it sizes the grid

@@ -49,6 +49,19 @@ def test_bounded_wait_check_validates_on_the_host(pa):
     assert L.pa_check_bounded_wait(1_000_000, 12, None) == pa.PA_ERR_INVALID_ARG
 
 
+def test_automatic_partition_size(pa):
+    # 1024 tokens once num_seqs * ceil(max_context_len / 1024) >= 64, else 512; explicit sizes pass through
+    assert pa.decode_partition_size(64, 4096) == 1024          # the 8B-shaped batch
+    assert pa.decode_partition_size(8, 131072) == 1024         # long context
+    assert pa.decode_partition_size(16, 4096) == 1024          # exactly 64 partitions
+    assert pa.decode_partition_size(15, 4096) == 512
+    assert pa.decode_partition_size(1, 20000) == 512
+    assert pa.decode_partition_size(10, 100, 256) == 256
+    # the workspace is sized for the partitions the call will use
+    assert pa.decode_workspace_bytes(64, 32, 128, 4096, 0) == pa.decode_workspace_bytes(64, 32, 128, 4096, 1024)
+    assert pa.decode_workspace_bytes(4, 32, 128, 4096, 0) == pa.decode_workspace_bytes(4, 32, 128, 4096, 512)
+
+
 def test_status_strings(pa):
     assert pa.status_string(0) == "PA_OK"
     assert pa.status_string(-5) == "PA_ERR_DEVICE_INDEX"
