@@ -109,7 +109,7 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
  * keep more, shorter partitions to spread over the SMs). max_context_len is the
  * call's bound (max_blocks_per_seq * block_size when the call passes 0).
  * Applies to pa_paged_attention_decode, _append, _noalloc and the _fp8 calls;
- * the sharing-aware decode uses 512 when given 0.
+ * the sharing-aware decode has its own rule (pa_decode_shared_partition_size).
  */
 int pa_decode_partition_size(int num_seqs, int max_context_len, int partition_size);
 
@@ -205,10 +205,24 @@ int pa_paged_attention_decode_append(void *out, const void *q, const void *k_new
  * Supported: dtype f16/bf16, head_dim 128, num_heads/num_kv_heads <= 16,
  * block_size a power of two in [8, 128], scale > 0. workspace >=
  * pa_decode_shared_workspace_bytes(...) bytes (NULL: taken with cudaMallocAsync
- * on the stream and released after the merge).
+ * on the stream and released after the merge). partition_size 0 = automatic
+ * (pa_decode_shared_partition_size); the shared and the per-sequence tokens use
+ * the same partition size.
  */
 size_t pa_decode_shared_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                         int max_context_len, int partition_size);
+
+/*
+ * The partition size a sharing-aware decode call uses: partition_size itself
+ * when it is not 0, else the multiple of 128 (at least 512, at most the longest
+ * shared prefix rounded up) that minimises an estimate of the shared pass's time
+ * on this device: ceil(items / SMs) x (128-key tiles per item + 1.4), items =
+ * num_groups x num_kv_heads x ceil(max_prefix_len / partition); ties go to the
+ * larger partition. With no groups or no shared tokens it is 512. Workspace
+ * sized by pa_decode_shared_workspace_bytes(..., 0) covers every automatic
+ * choice. Reads the current device's SM count (152 when it cannot be read).
+ */
+int pa_decode_shared_partition_size(int num_groups, int num_kv_heads, int max_prefix_len, int partition_size);
 
 int pa_paged_attention_decode_shared(void *out, const void *q, const void *key_cache,
                                      const void *value_cache, const int32_t *block_tables,

@@ -12,12 +12,16 @@
 // Work item = (sequence, kv head, tile of query tokens). The item's 128 MMA
 // rows are (query token, head of the group) pairs: QT = 128 / Gp tokens x Gp
 // heads, Gp = G rounded up to a power of two. Per tile of 128 keys:
-//   S[128 rows x 128 keys] = Q . K^T    (tcgen05 kind::f16, M=128 N=128 K=128)
+//   S[128 rows x 128 keys] = Q . K^T    (tcgen05 kind::f16, M=128 N=128 K=128,
+//                                        Q from tensor memory, K from shared memory)
 //   O[128 rows x 128 dims] += P . V     (P from tensor memory, V MN-major)
-// S is double-buffered and O stays in tensor memory; P is written by the softmax
-// threads into tensor memory (each thread's row is its lane: 16-bit pairs, two
-// 64-column buffers), where the P.V MMA takes its A operand -- no shared-memory
-// round trip for P (all 512 columns in use).
+// Tensor memory (512 columns): S double-buffered (256), O (128), the item's query
+// rows Q (64, 16-bit pairs per lane) and P (64, 16-bit pairs per lane). With both
+// operands of the S MMA in shared memory, it and the TMA writes of each tile's K
+// and V moved about 160 KB of shared memory per tile; with Q in tensor memory the S
+// MMA reads only K. P is written by the softmax threads (each thread's row is its
+// lane), where the P.V MMA takes its A operand, so P makes no shared-memory round
+// trip; it is single-buffered: tile j's softmax writes it once P(j-1).V has run.
 // Thread = row for the softmax, so the max and the sum are thread-local; O is
 // rescaled (tcgen05.ld / st of the row) only when a row's max grows by more than
 // 2^8, otherwise the stale reference max is kept (the final O / l is the same).
@@ -25,9 +29,8 @@
 // relative difference of at most 2^-9 per weight, of either sign). The exponent
 // arguments and the sums use the paired fp32 instructions (two lanes each).
 //
-// Roles (224 threads, one persistent CTA per SM):
-//   warp 0     TMA: the item's query rows (3-D map over [tokens, heads, dims]),
-//              then per key tile the K boxes of each physical block into a
+// Roles (256 threads, one persistent CTA per SM):
+//   warp 0     TMA: per key tile the K boxes of each physical block into a
 //              2-stage K ring.
 //   warp 6     TMA: the V boxes of every key tile into a 2-stage V ring with its
 //              own barriers (K freed after its S MMA, V after its P.V MMA). Each
@@ -35,9 +38,15 @@
 //              blocks past the last visible key load from an out-of-range
 //              coordinate (zeros). With one producer warp for both operands the
 //              producer was busy 95 % of the time and the MMA waited on K.
+//   warp 7     TMA: each item's query rows (3-D map over [tokens, heads, dims];
+//              group mode: one 2-D box per member) into shared memory, as soon
+//              as the previous item's rows have moved to tensor memory.
 //   warp 1     one thread issues the MMAs and owns tensor memory.
 //   warps 2-5  softmax (scale, causal mask, exp2, P to tensor memory, V rows of
-//              keys past the last visible one zeroed) and the epilogue O / l.
+//              keys past the last visible one zeroed), the copy of the next
+//              item's query rows from shared to tensor memory once this item's
+//              last S has been read (its S MMAs then run during this epilogue),
+//              and the epilogue O / l.
 // Items differ in size by up to the context length (key tiles = causal extent
 // / 128), and a persistent CTA ends with its last item: dealt in index order the
 // most loaded CTA of the chunked-prefill batch had 13 % more key tiles than the
@@ -66,22 +75,25 @@ using namespace prefill;
 
 constexpr int kD = 128;
 constexpr int kRows = 128;                     // MMA rows per item
-constexpr int kStages = 2;
+constexpr int kKStages = 2;                    // K ring
+constexpr int kVStages = 2;                    // V ring
 constexpr int kChunk = 128 * 128;              // 128 rows x 128 bytes (one 64-element half)
 constexpr int kKVBytes = 2 * kChunk;           // one K (or V) tile
 constexpr int kQBytes = 2 * kChunk;
-constexpr int kThreads = 224;                  // + warp 6: V producer
+constexpr int kThreads = 256;                  // + warp 6: V producer, warp 7: Q producer
 constexpr int kVProdWarp = 6;
-constexpr uint32_t kTmemCols = 512;            // S[2] x 128 + O x 128 + P[2] x 64
+constexpr int kQProdWarp = 7;
+constexpr uint32_t kTmemCols = 512;            // S[2] x 128 + O x 128 + Q x 64 + P x 64
 constexpr uint32_t kColO = 2 * kKT;
-constexpr uint32_t kColP = 3 * kKT;            // P[2]: 64 columns each, 16-bit pairs per lane (row)
+constexpr uint32_t kColQ = 3 * kKT;            // the item's query rows: 16-bit pairs per lane (row)
+constexpr uint32_t kColP = 3 * kKT + 64;       // P: 64 columns, 16-bit pairs per lane (row)
 constexpr float kRescaleLog2 = 8.f;            // keep the reference max until a row's max grows by 2^8
 
 constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kStages * kKVBytes;
-constexpr int kOffQ = kOffV + kStages * kKVBytes;
+constexpr int kOffV = kOffK + kKStages * kKVBytes;
+constexpr int kOffQ = kOffV + kVStages * kKVBytes;
 constexpr int kOffBar = kOffQ + kQBytes;
-constexpr int kNumBars = 19;
+constexpr int kNumBars = 22;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kMaxMyItems = 1024;              // a CTA's items after the sort
 constexpr int kOffMy = kOffMisc + 16;          // int [kMaxMyItems]: this CTA's items, in order
@@ -123,9 +135,9 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
     uint64_t *bb = reinterpret_cast<uint64_t *>(smem + kOffBar);
     // K and V stages have separate barriers: a K stage is free again as soon as its
     // S MMA is done, a V stage only after its P.V MMA.
-    uint64_t *k_full = bb, *k_empty = bb + 2, *v_full = bb + 4, *v_empty = bb + 6;
-    uint64_t *s_full = bb + 8, *s_free = bb + 10, *p_full = bb + 12, *o_done = bb + 14;
-    uint64_t *q_full = bb + 16, *q_empty = bb + 17, *o_free = bb + 18;
+    uint64_t *k_full = bb, *k_empty = bb + 3, *v_full = bb + 6, *v_empty = bb + 8;
+    uint64_t *s_full = bb + 10, *s_free = bb + 12, *p_full = bb + 14, *o_done = bb + 16;
+    uint64_t *q_full = bb + 18, *q_empty = bb + 19, *o_free = bb + 20, *q_tm = bb + 21;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -135,9 +147,11 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                                    : p.num_seqs * p.num_kv_heads * p.qtiles;
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
@@ -146,7 +160,8 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
             mbar_init(&o_done[i], 1);
         }
         mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
+        mbar_init(q_empty, 4);           // the softmax warps, the rows copied to tensor memory
+        mbar_init(q_tm, 4);              // the same arrivals: Q is in tensor memory
         mbar_init(o_free, 4);
         *abort_flag = 0;
         mbar_fence_init();
@@ -188,47 +203,23 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
     auto item_at = [&](int k) { return use_list ? my_items[k] : (int)blockIdx.x + k * (int)gridDim.x; };
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer: Q and K
-        // Per item: the query rows, then per key tile its K boxes. The item's block
-        // ids are read once at item start.
+        // ------------------------------------------------------------ TMA producer: K
+        // Per key tile its K boxes, into a 3-stage ring. The item's block ids are read
+        // once at item start.
         const int nbt = kKT / p.block_size;
-        uint32_t it = 0, n = 0;                         // K tiles, items issued
+        uint32_t it = 0;                                // K tiles issued
         bool ok = true;
         for (int k = 0; k < nloop && ok; ++k) {
             const int idx = item_at(k);
             PItem I;
             if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
             const KeyTable tb = load_key_table(p, I, lane);
-            int w = 1;
-            if (lane == 0) {
-                w = mbar_wait(q_empty, (n & 1) ^ 1) ? 1 : 0;
-                if (w) {
-                    mbar_arrive_expect_tx(q_full, kQBytes);
-                    if constexpr (kGroup) {
-                        // one box of Gp head rows per member slot; empty slots read zeros
-                        const int32_t *mem = p.group_members + (int64_t)I.group * p.max_members;
-                        for (int m = 0; m < p.rows_q; ++m) {
-                            const int row = m < I.members ? mem[m] * p.num_heads + I.kvh * G
-                                                          : p.num_seqs * p.num_heads;
-                            tma_load_2d(sQ + m * Gp * 128, &tm_q, q_full, 0, row);
-                            tma_load_2d(sQ + kChunk + m * Gp * 128, &tm_q, q_full, 64, row);
-                        }
-                    } else {
-                        tma_load_3d(sQ, &tm_q, q_full, 0, I.kvh * G, I.q_row0);
-                        tma_load_3d(sQ + kChunk, &tm_q, q_full, 64, I.kvh * G, I.q_row0);
-                    }
-                }
-            }
-            w = __shfl_sync(0xffffffffu, w, 0);
-            if (!w) {
-                ok = false;
-                break;
-            }
-            ++n;
             for (int j = 0; j < I.ntiles; ++j, ++it) {
-                const int stage = it & 1;
+                const int stage = it % kKStages;
+                const uint32_t ph = (it / kKStages) & 1;
                 const int phys = tile_block(tb, p, j, nbt, lane, true);
-                if (lane == 0) w = mbar_wait(&k_empty[stage], ((it >> 1) & 1) ^ 1) ? 1 : 0;
+                int w = 1;
+                if (lane == 0) w = mbar_wait(&k_empty[stage], ph ^ 1) ? 1 : 0;
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (!w || *abort_flag) {
                     ok = false;
@@ -247,10 +238,46 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
             *abort_flag = 1;
             raise_error(p.err, PA_DEVERR_WAIT);
         }
-        if (lane == 0) {   // drain copies in flight
-            for (uint32_t j = it > 2u ? it - 2 : 0; j < it; ++j) mbar_wait(&k_full[j & 1], (j >> 1) & 1);
-            if (n > 0) mbar_wait(q_full, (n - 1) & 1);
+        if (lane == 0)   // drain copies in flight
+            for (uint32_t j = it > (uint32_t)kKStages ? it - kKStages : 0; j < it; ++j)
+                mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1);
+    } else if (warp == kQProdWarp) {
+        // ------------------------------------------------------------ TMA producer: Q
+        // Each item's query rows as soon as the previous item's rows have gone to tensor
+        // memory, so the load overlaps the item before.
+        if (lane == 0) {
+            uint32_t n = 0;                             // items issued
+            bool ok = true;
+            for (int k = 0; k < nloop && ok; ++k) {
+                const int idx = item_at(k);
+                PItem I;
+                if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
+                if (*abort_flag || !mbar_wait(q_empty, (n & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(q_full, kQBytes);
+                if constexpr (kGroup) {
+                    // one box of Gp head rows per member slot; empty slots read zeros
+                    const int32_t *mem = p.group_members + (int64_t)I.group * p.max_members;
+                    for (int m = 0; m < p.rows_q; ++m) {
+                        const int row = m < I.members ? mem[m] * p.num_heads + I.kvh * G : p.num_seqs * p.num_heads;
+                        tma_load_2d(sQ + m * Gp * 128, &tm_q, q_full, 0, row);
+                        tma_load_2d(sQ + kChunk + m * Gp * 128, &tm_q, q_full, 64, row);
+                    }
+                } else {
+                    tma_load_3d(sQ, &tm_q, q_full, 0, I.kvh * G, I.q_row0);
+                    tma_load_3d(sQ + kChunk, &tm_q, q_full, 64, I.kvh * G, I.q_row0);
+                }
+                ++n;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                raise_error(p.err, PA_DEVERR_WAIT);
+            }
+            if (n > 0) mbar_wait(q_full, (n - 1) & 1);   // drain the copy in flight
         }
+        __syncwarp();
     } else if (warp == kVProdWarp) {
         // ------------------------------------------------------------ TMA producer: V
         const int nbt = kKT / p.block_size;
@@ -292,7 +319,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
             constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
             const uint32_t idesc_s = instr_desc_f16(kRows, kKT, kBf16, false, false);
             const uint32_t idesc_o = instr_desc_f16(kRows, kD, kBf16, false, true);
-            const uint32_t sK0 = smem_addr(sK), sV0 = smem_addr(sV), sQ0 = smem_addr(sQ);
+            const uint32_t sK0 = smem_addr(sK), sV0 = smem_addr(sV);
             uint32_t it = 0, n = 0;
             bool ok = true;
             // O += P(j) V(j); `first` starts the item's accumulator
@@ -305,7 +332,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
 #pragma unroll
                 for (int kk = 0; kk < kKT / 16; ++kk) {
                     const uint64_t b = smem_desc(vb + kk * 2048, kChunk, 1024);
-                    mma_f16_tmem_a(tmem + kColO, tmem + kColP + (j & 1) * 64 + kk * 8, b, idesc_o,
+                    mma_f16_tmem_a(tmem + kColO, tmem + kColP + kk * 8, b, idesc_o,
                                    (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(&o_done[j & 1]);
@@ -316,29 +343,29 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                 const int idx = item_at(k);
                 PItem I;
                 if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
-                if (!mbar_wait(q_full, n & 1)) {
+                if (!mbar_wait(q_tm, n & 1)) {
                     ok = false;
                     break;
                 }
                 ++n;
                 for (int j = 0; j < I.ntiles; ++j, ++it) {
-                    const int stage = it & 1;
-                    if (*abort_flag || !mbar_wait(&k_full[stage], (it >> 1) & 1) ||
+                    const int stage = it & 1;                 // S buffer
+                    const int kst = it % kKStages;            // K stage
+                    if (*abort_flag || !mbar_wait(&k_full[kst], (it / kKStages) & 1) ||
                         !mbar_wait(&s_free[stage], ((it >> 1) & 1) ^ 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t kb = sK0 + stage * kKVBytes;
+                    const uint32_t kb = sK0 + kst * kKVBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
+                    for (int kk = 0; kk < kD / 16; ++kk) {       // A = Q from tensor memory, B = K
                         const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-                        mma_f16(tmem + stage * kKT, smem_desc(sQ0 + off, 16, 1024), smem_desc(kb + off, 16, 1024),
-                                idesc_s, kk > 0);
+                        mma_f16_tmem_a(tmem + stage * kKT, tmem + kColQ + kk * 8, smem_desc(kb + off, 16, 1024),
+                                       idesc_s, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&s_full[stage]);
-                    mma_commit(&k_empty[stage]);
-                    if (j == I.ntiles - 1) mma_commit(q_empty);
+                    mma_commit(&k_empty[kst]);
                     if (j > 0 && !issue_pv(it - 1, j == 1)) {
                         ok = false;
                         break;
@@ -366,10 +393,46 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
         T *out = reinterpret_cast<T *>(p.out);
         uint32_t it = 0, n = 0;
         bool ok = true;
+        // Item n's query rows, from the TMA tile in shared memory (128-byte rows, 16-byte
+        // chunks rotated by row) to Q in tensor memory, where the S MMAs take their A
+        // operand; then the shared tile is free for the next item's rows.
+        auto copy_q = [&](uint32_t nq_idx) -> bool {
+            if (!warp_wait(q_full, nq_idx & 1)) return false;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint4 *row = reinterpret_cast<const uint4 *>(sQ + h * kChunk + r * 128);
+                uint32_t qv[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = row[c ^ (r & 7)];
+                    qv[4 * c] = x.x;
+                    qv[4 * c + 1] = x.y;
+                    qv[4 * c + 2] = x.z;
+                    qv[4 * c + 3] = x.w;
+                }
+                tmem_st32(tmem + lane_off + kColQ + h * 32, qv);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(q_empty);
+                mbar_arrive(q_tm);
+            }
+            return true;
+        };
+        auto valid_item = [&](int kk) {
+            PItem J;
+            return kGroup ? get_gitem(item_at(kk), p, J) : get_pitem(item_at(kk), p, J);
+        };
         for (int k = 0; k < nloop && ok; ++k) {
             const int idx = item_at(k);
             PItem I;
             if (!(kGroup ? get_gitem(idx, p, I) : get_pitem(idx, p, I))) continue;
+            if (n == 0 && !copy_q(0)) {
+                ok = false;
+                break;
+            }
             const bool row_valid = qi < I.nq && g < G;
             // causal position (prefill), or the last shared key (group mode: no causal limit)
             const int pos = !row_valid ? -1 : (kGroup ? I.kmax - 1 : I.pos_first + qi);
@@ -430,8 +493,8 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                     }
                     tmem_wait_st();
                 }
-                // P buffer `buf` was last read by the MMA of tile it-2
-                if (it >= 2 && !warp_wait(&o_done[buf], ((it - 2) >> 1) & 1)) {
+                // P was last read by the MMA of tile it-1
+                if (it >= 1 && !warp_wait(&o_done[(it - 1) & 1], ((it - 1) >> 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -450,7 +513,7 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                         pw[q] = pack2<T>(pv.x, pv.y);
                         ls2[q & 1] = fadd2(ls2[q & 1], pv);
                     }
-                    tmem_st32(tmem + lane_off + kColP + buf * 64 + h * 32, pw);
+                    tmem_st32(tmem + lane_off + kColP + h * 32, pw);
                 }
                 tmem_wait_st();
                 l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
@@ -475,6 +538,16 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                 if (lane == 0) mbar_arrive(&p_full[buf]);
             }
             if (!ok) break;
+            // The next item's query rows, now that every S MMA of this one has run: its S
+            // MMAs then proceed during this epilogue.
+            {
+                int k2 = k + 1;
+                while (k2 < nloop && !valid_item(k2)) ++k2;
+                if (k2 < nloop && !copy_q(n + 1)) {
+                    ok = false;
+                    break;
+                }
+            }
             // ---- epilogue: O / l of this item's rows
             const uint32_t last = it - 1;
             if (!warp_wait(&o_done[last & 1], (last >> 1) & 1)) {

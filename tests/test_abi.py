@@ -62,6 +62,38 @@ def test_automatic_partition_size(pa):
     assert pa.decode_workspace_bytes(4, 32, 128, 4096, 0) == pa.decode_workspace_bytes(4, 32, 128, 4096, 512)
 
 
+def _shared_rule(groups, kvh, max_prefix, sms=152):
+    # the documented estimate: ceil(items / SMs) * (tiles per item + 1.4), minimised
+    # over multiples of 128 from 512 to the longest prefix, ties to the larger
+    if groups <= 0 or kvh <= 0 or max_prefix <= 0:
+        return 512
+    best, best_cost = None, None
+    top = max(min(-(-max_prefix // 128) * 128, 65536), 512)
+    for part in range(512, top + 1, 128):
+        items = groups * kvh * -(-max_prefix // part)
+        cost = -(-items // sms) * (-(-min(part, max_prefix) // 128) + 1.4)
+        if best is None or cost <= best_cost:
+            best, best_cost = part, cost
+    return best
+
+
+def test_automatic_shared_partition_size(pa):
+    # the forked-sampling batch: 32 prompts of 992 shared tokens, 8 kv heads -> one
+    # partition per (group, kv head)
+    assert pa.decode_shared_partition_size(32, 8, 992) == 1024
+    assert pa.decode_shared_partition_size(0, 8, 992) == 512           # no groups
+    assert pa.decode_shared_partition_size(32, 8, 0) == 512            # nothing shared
+    assert pa.decode_shared_partition_size(32, 8, 992, 256) == 256     # explicit sizes pass through
+    assert pa.decode_shared_partition_size(32, 8, 300) == 512          # never below 512
+    for groups, kvh, prefix in [(1, 8, 32768), (32, 8, 32768), (4, 1, 5000), (200, 8, 4096), (3, 2, 100000)]:
+        got = pa.decode_shared_partition_size(groups, kvh, prefix)
+        assert got == _shared_rule(groups, kvh, prefix), (groups, kvh, prefix, got)
+        assert got % 128 == 0 and got >= 512
+        # the workspace sized for the automatic choice (0) covers it
+        assert pa.decode_shared_workspace_bytes(64, 32, 128, prefix + 4096, 0) >= \
+            pa.decode_shared_workspace_bytes(64, 32, 128, prefix + 4096, got)
+
+
 def test_status_strings(pa):
     assert pa.status_string(0) == "PA_OK"
     assert pa.status_string(-5) == "PA_ERR_DEVICE_INDEX"

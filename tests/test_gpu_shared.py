@@ -81,6 +81,26 @@ def test_shared_prefix_sampling_reads_prompts_once(pa):
     assert_close(b[seqs], ref, "bf16", "shared-prefix decode")
 
 
+@pytest.mark.parametrize("partition", [0, 896, 2048])
+def test_shared_prefix_batch_partition_sizes(pa, partition):
+    """The bench's forked-sampling batch (32 prompts x 8 samples): the automatic
+    partition (one per group and kv head, 1024 tokens) and explicit sizes that split
+    the 992 shared tokens unevenly (896 + 96) or cover shared and private tokens
+    alike (2048)."""
+    sc, w = _shared_prefix_state(num_prompts=32)
+    pl, gm = pa.prefix_groups(w.block_tables, w.context_lens, w.block_size, 8)
+    if partition == 0:
+        assert pa.decode_shared_partition_size(gm.shape[0], w.num_kv_heads, int(pl.max())) == 1024
+    plain, shared, pl, gm = _run(pa, w, max_members=8, partition_size=partition)
+    assert pa.get_device_error() == 0
+    b = to_f64(shared)
+    assert np.all(np.isfinite(b))
+    assert np.abs(to_f64(plain) - b).max() <= 2e-2
+    seqs = np.arange(1, w.num_seqs, 5)
+    w.slot_mapping = np.full(w.num_seqs, -1, np.int32)             # contents already complete
+    assert_close(b[seqs], _oracle_full(w, seqs), "bf16", f"shared-prefix batch, partition {partition}")
+
+
 def _oracle_full(w, seqs):
     view = w.compact_host_view(seqs, include_newest=True)
     kc = workloads.to_storage_numpy(view["key_cache"], w.dtype)
