@@ -369,8 +369,8 @@ class Step:
                 "write": ("fused: decode with append (each sequence's new token written by the decode kernel)"
                           if self.append else "separate scatter launch"),
                 "copied_blocks": 0 if self.copy_pairs is None else int(self.copy_pairs.shape[0]),
-                "partition_size": (self.pa.decode_shared_partition_size(int(self.shared[1].shape[0]), w.num_kv_heads,
-                                                                        self.shared[2])
+                "partition_size": (self.pa.decode_shared_partition_size(w.num_seqs, int(self.shared[1].shape[0]),
+                                                                        w.num_kv_heads, self.shared[2], self.max_ctx)
                                    if self.shared is not None else
                                    self.pa.decode_partition_size(w.num_seqs, self.max_ctx, self.part)),
                 "shared_prefix_decode": self.shared is not None,

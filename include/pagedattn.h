@@ -218,11 +218,18 @@ size_t pa_decode_shared_workspace_bytes(int num_seqs, int num_heads, int head_di
  * shared prefix rounded up) that minimises an estimate of the shared pass's time
  * on this device: ceil(items / SMs) x (128-key tiles per item + 1.4), items =
  * num_groups x num_kv_heads x ceil(max_prefix_len / partition); ties go to the
- * larger partition. With no groups or no shared tokens it is 512. Workspace
- * sized by pa_decode_shared_workspace_bytes(..., 0) covers every automatic
- * choice. Reads the current device's SM count (152 when it cannot be read).
+ * larger partition. When that holds each shared prefix in one partition, the
+ * result grows to max_context_len rounded up to 128 if that is at most 8192 and
+ * num_seqs x num_kv_heads >= 2 x SMs. With no groups or no shared tokens it is
+ * 512. max_context_len: the call's bound (max_blocks_per_seq * block_size when the
+ * call passes 0). A call whose partition is >= that bound (with at most 8 query
+ * heads per kv head) runs no merge: the per-sequence pass joins the shared
+ * partial itself. Workspace sized by
+ * pa_decode_shared_workspace_bytes(..., 0) covers every automatic choice. Reads
+ * the current device's SM count (152 when it cannot be read).
  */
-int pa_decode_shared_partition_size(int num_groups, int num_kv_heads, int max_prefix_len, int partition_size);
+int pa_decode_shared_partition_size(int num_seqs, int num_groups, int num_kv_heads, int max_prefix_len,
+                                    int max_context_len, int partition_size);
 
 int pa_paged_attention_decode_shared(void *out, const void *q, const void *key_cache,
                                      const void *value_cache, const int32_t *block_tables,

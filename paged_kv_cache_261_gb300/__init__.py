@@ -76,7 +76,7 @@ _decl("pa_version", [])
 _decl("pa_paged_kv_write", [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp])
 _decl("pa_decode_workspace_bytes", [_i32, _i32, _i32, _i32, _i32], _sz)
 _decl("pa_decode_partition_size", [_i32, _i32, _i32])
-_decl("pa_decode_shared_partition_size", [_i32, _i32, _i32, _i32])
+_decl("pa_decode_shared_partition_size", [_i32, _i32, _i32, _i32, _i32, _i32])
 _decl("pa_paged_attention_decode", [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                     _i64, _f, _i32, _i32, _vp, _sz, _i32, _vp])
 _decl("pa_paged_attention_decode_append", [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
@@ -202,10 +202,11 @@ def decode_partition_size(num_seqs: int, max_context_len: int, partition_size: i
     return int(_lib.pa_decode_partition_size(num_seqs, max_context_len, partition_size))
 
 
-def decode_shared_partition_size(num_groups: int, num_kv_heads: int, max_prefix_len: int,
-                                 partition_size: int = 0) -> int:
+def decode_shared_partition_size(num_seqs: int, num_groups: int, num_kv_heads: int, max_prefix_len: int,
+                                 max_context_len: int, partition_size: int = 0) -> int:
     """Partition size (tokens) a sharing-aware decode call uses: partition_size, or the automatic choice for 0."""
-    return int(_lib.pa_decode_shared_partition_size(num_groups, num_kv_heads, max_prefix_len, partition_size))
+    return int(_lib.pa_decode_shared_partition_size(num_seqs, num_groups, num_kv_heads, max_prefix_len,
+                                                    max_context_len, partition_size))
 
 
 def _workspace(device, stream_ptr: int, nbytes: int):

@@ -96,8 +96,13 @@ int device_sm_count() {
 // (tiles + 1.4) is minimised over multiples of 128 from 512 up to the longest shared
 // prefix, ties going to the larger partition (fewer partials to merge). Measured on
 // the forked-sampling batch (32 prompts of 992 shared tokens, 8 samples each, G 4):
-// 512 -> 0.0855 ms, 896 -> 0.0998 ms, 1024 -> 0.0803 ms (the choice), 2048 ->
-// 0.0796 ms; the private pass uses the same partition.
+// 512 -> 0.0855 ms, 896 -> 0.0998 ms, 1024 -> 0.0803 ms, 2048 -> 0.0796 ms; the
+// private pass uses the same partition. When the choice already holds each shared
+// prefix in one partition, the partition grows to cover every whole context (the
+// shared pass is unchanged) as long as that stays within kFoldMaxContext tokens and
+// the private pass keeps two items per SM: then no merge runs (fold_shared).
+constexpr int64_t kFoldMaxContext = 8192;
+
 int shared_partition(int64_t num_groups, int64_t num_kv_heads, int64_t max_prefix, int sms) {
     if (num_groups <= 0 || num_kv_heads <= 0 || max_prefix <= 0 || sms <= 0) return kSharedPartition;
     const int64_t top = std::min<int64_t>((max_prefix + 127) / 128 * 128, 65536);
@@ -440,9 +445,21 @@ int pa_paged_attention_decode_fp8_append(void *out, const void *q, const void *k
                            workspace_bytes, dtype, stream);
 }
 
-int pa_decode_shared_partition_size(int num_groups, int num_kv_heads, int max_prefix_len, int partition_size) {
+int shared_partition_for(int64_t num_seqs, int64_t num_groups, int64_t num_kv_heads, int64_t max_prefix,
+                         int64_t max_ctx, int sms) {
+    int part = shared_partition(num_groups, num_kv_heads, max_prefix, sms);
+    const int64_t whole = (max_ctx + 127) / 128 * 128;
+    if (num_groups > 0 && max_prefix > 0 && part >= max_prefix && whole > part && whole <= kFoldMaxContext &&
+        num_seqs * num_kv_heads >= 2 * (int64_t)sms)
+        part = (int)whole;
+    return part;
+}
+
+int pa_decode_shared_partition_size(int num_seqs, int num_groups, int num_kv_heads, int max_prefix_len,
+                                    int max_context_len, int partition_size) {
     if (partition_size != 0) return partition_size;
-    return shared_partition(num_groups, num_kv_heads, max_prefix_len, device_sm_count());
+    return shared_partition_for(num_seqs, num_groups, num_kv_heads, max_prefix_len, max_context_len,
+                                device_sm_count());
 }
 
 size_t pa_decode_shared_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
@@ -480,9 +497,9 @@ int pa_paged_attention_decode_shared(void *out, const void *q, const void *key_c
     const int64_t max_ctx = max_context_len == 0 ? table_cap : max_context_len;
     if (max_ctx > INT32_MAX || num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
     const int part = partition_size != 0 ? partition_size
-                                         : shared_partition(num_groups, num_kv_heads,
-                                                            std::min<int64_t>(max_prefix_len, max_ctx),
-                                                            device_sm_count());
+                                         : shared_partition_for(num_seqs, num_groups, num_kv_heads,
+                                                                std::min<int64_t>(max_prefix_len, max_ctx), max_ctx,
+                                                                device_sm_count());
     const int64_t P = num_partitions(max_ctx, part) + 1;
     if (P > INT32_MAX / part) return PA_ERR_UNSUPPORTED;
     int64_t limit = (P - 1) * part < table_cap ? (P - 1) * part : table_cap;
@@ -509,6 +526,9 @@ int pa_paged_attention_decode_shared(void *out, const void *q, const void *key_c
     d.max_partitions = (int)P;
     d.context_limit = (int)limit;
     d.scale_log2 = scale * pa::kLog2e;
+    // one partition covers every whole context: the private pass folds the shared
+    // partials and writes the final rows, and no merge runs
+    d.fold_shared = part >= max_ctx && d.group <= 8 ? 1 : 0;
     if (!pa::decode_tc_supported(d, dtype)) return PA_ERR_UNSUPPORTED;
     if (int rc = error_word(&d.err)) return rc;
 
@@ -564,7 +584,7 @@ int pa_paged_attention_decode_shared(void *out, const void *q, const void *key_c
     int rc = 0;
     if (num_groups > 0 && g.shared_parts > 0) rc = pa::launch_shared_prefix_tc(g, dtype, s);
     if (rc == 0) rc = pa::launch_decode_tc(d, dtype, s);
-    if (rc == 0) rc = pa::launch_decode_reduce(d, dtype, s);
+    if (rc == 0 && !d.fold_shared) rc = pa::launch_decode_reduce(d, dtype, s);
     if (owned) cudaFreeAsync(ws, s);
     if (rc == -2) return PA_ERR_UNSUPPORTED;
     return rc == 0 ? PA_OK : PA_ERR_CUDA;

@@ -93,9 +93,11 @@ __device__ __forceinline__ void build(const DecodeParams &p, int *prefix, int *o
         const int rt = (len - nfull * p.partition_size + kTile - 1) / kTile;   // tiles of the ragged rest
         const bool rest_is_full = rt * kTile == p.partition_size;           // as many tiles as a full one
         prefix[b + 1] = nfull + (rest_is_full ? 1 : 0);
-        // list bucket: 0 = empty context, 1..3 = tiles of the rest (3 = three or more),
-        // 4 = no list entry (no ragged rest, or one with the full tile count)
-        code[b] = (unsigned char)(sp.ctx == 0 ? 0 : ((rt == 0 || rest_is_full) ? 4 : min(rt, 3)));
+        // list bucket: 0 = empty context (or, when folding, a wholly shared one: an item
+        // with no tiles), 1..3 = tiles of the rest (3 = three or more), 4 = no list entry
+        // (no ragged rest, or one with the full tile count)
+        const bool empty = sp.ctx == 0 || (p.fold_shared && len == 0);
+        code[b] = (unsigned char)(empty ? 0 : ((rt == 0 || rest_is_full) ? 4 : min(rt, 3)));
     }
     __syncthreads();
     if (warp == 0) {

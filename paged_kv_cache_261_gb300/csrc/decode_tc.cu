@@ -184,7 +184,7 @@ template <> __device__ __forceinline__ float from_bits<__half>(uint16_t b) {
     return __half2float(__ushort_as_half(b));
 }
 
-template <typename T, int GT>
+template <typename T, int GT, bool kFold>
 __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                 const __grid_constant__ CUtensorMap tm_v,
                                                                 const __grid_constant__ CUtensorMap tm_q,
@@ -477,7 +477,22 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         for (int k = 0; k < nmy && ok; ++k) {
             const Item I = decode_order::unpack_item(items[k]);
             const int64_t head0 = (int64_t)I.b * p.num_heads + (int64_t)I.kvh * G;
-            if (I.ntiles == 0) {
+            // joining the shared pass's partial (kFold: one slot, since one partition
+            // covers the whole context): loaded now so the loads overlap the tiles
+            const bool fold = kFold && I.slot > 0;
+            float f_m[kC], f_l[kC], f_o[kC];
+            if constexpr (kFold) {
+                if (fold) {
+#pragma unroll
+                    for (int u = 0; u < kC; ++u) {
+                        const int64_t r0 = (head0 + (c0 + u < G ? c0 + u : 0)) * p.max_partitions;
+                        f_m[u] = p.ws_ml[2 * r0];
+                        f_l[u] = p.ws_ml[2 * r0 + 1];
+                        f_o[u] = p.ws_o[r0 * kD + row];
+                    }
+                }
+            }
+            if (I.ntiles == 0 && !fold) {
 #pragma unroll
                 for (int u = 0; u < kC; ++u)
                     if (c0 + u < G) out[(head0 + c0 + u) * kD + row] = Elem<T>::from_f(0.f);
@@ -576,7 +591,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                 for (int u = 0; u < kC; ++u) alpha_prev[u] = alpha[u];
             }
             if (!ok) break;
-            if (!accumulate(it - 1)) {
+            if ((!kFold || I.ntiles > 0) && !accumulate(it - 1)) {
                 ok = false;
                 break;
             }
@@ -600,7 +615,20 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
                 const int g = c0 + u;
                 l_tot[u] = lr[g] + lr[kN + g] + lr[2 * kN + g] + lr[3 * kN + g];
             }
-            if (I.direct) {
+            if (fold) {
+                // the shared pass's partial of these heads (slot 0, written before this
+                // kernel) joined with this item's: one softmax over the whole context
+#pragma unroll
+                for (int u = 0; u < kC; ++u) {
+                    if (c0 + u < G) {
+                        const float M = fmaxf(m_run[u], f_m[u]);
+                        const float f = m_run[u] == -INFINITY ? 0.f : fast_exp2(m_run[u] - M);
+                        const float fs = f_m[u] == -INFINITY ? 0.f : fast_exp2(f_m[u] - M);
+                        const float num = fmaf(f_o[u], fs, o_acc[u] * f), den = fmaf(f_l[u], fs, l_tot[u] * f);
+                        out[(head0 + c0 + u) * kD + row] = Elem<T>::from_f(num / den);
+                    }
+                }
+            } else if (I.direct) {
 #pragma unroll
                 for (int u = 0; u < kC; ++u)
                     if (c0 + u < G) out[(head0 + c0 + u) * kD + row] = Elem<T>::from_f(o_acc[u] / l_tot[u]);
@@ -652,9 +680,9 @@ bool make_q_map(CUtensorMap *m, const DecodeParams &p, CUtensorMapDataType dt) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int GT>
+template <typename T, int GT, bool kFold>
 int launch_tc_t(const DecodeParams &p, CUtensorMapDataType dt, cudaStream_t stream) {
-    auto kern = decode_tc_kernel<T, GT>;
+    auto kern = decode_tc_kernel<T, GT, kFold>;
     static bool attr_set[kMaxDevices] = {};
     static int num_sms[kMaxDevices] = {};
     int dev = 0;
@@ -674,11 +702,18 @@ int launch_tc_t(const DecodeParams &p, CUtensorMapDataType dt, cudaStream_t stre
     return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, stream, mk, mv, mq, p);
 }
 
+// The joining instance (fold_shared) exists for groups of up to 8 heads; the host sets
+// fold_shared only there.
 template <typename T>
 int launch_tc_g(const DecodeParams &p, CUtensorMapDataType dt, cudaStream_t stream) {
-    if (p.group <= 4) return launch_tc_t<T, 4>(p, dt, stream);
-    if (p.group <= 8) return launch_tc_t<T, 8>(p, dt, stream);
-    return launch_tc_t<T, 16>(p, dt, stream);
+    if (p.fold_shared) {
+        if (p.group <= 4) return launch_tc_t<T, 4, true>(p, dt, stream);
+        if (p.group <= 8) return launch_tc_t<T, 8, true>(p, dt, stream);
+        return -2;
+    }
+    if (p.group <= 4) return launch_tc_t<T, 4, false>(p, dt, stream);
+    if (p.group <= 8) return launch_tc_t<T, 8, false>(p, dt, stream);
+    return launch_tc_t<T, 16, false>(p, dt, stream);
 }
 
 }  // namespace

@@ -39,6 +39,12 @@ struct DecodeParams {
     int max_partitions;        // P: partitions per sequence the grid covers
     int context_limit;         // min(max_blocks_per_seq*bs, P*partition_size)
     float scale_log2;          // scale * log2(e)
+    // Sharing-aware decode with one partition covering every whole context (each
+    // sequence: at most one shared and one private partition): the tensor-core kernel's
+    // item for a sequence's tokens after its shared prefix joins the shared pass's
+    // partial (slot 0) with its own and writes the final row, so no merge runs; a
+    // sequence whose whole context is shared gets an item with no tiles that only joins.
+    int fold_shared;
 };
 
 // Chunked prefill: every query row of a packed chunk attends causally.

@@ -62,9 +62,10 @@ def test_automatic_partition_size(pa):
     assert pa.decode_workspace_bytes(4, 32, 128, 4096, 0) == pa.decode_workspace_bytes(4, 32, 128, 4096, 512)
 
 
-def _shared_rule(groups, kvh, max_prefix, sms=152):
+def _shared_rule(num_seqs, groups, kvh, max_prefix, max_ctx, sms=152):
     # the documented estimate: ceil(items / SMs) * (tiles per item + 1.4), minimised
-    # over multiples of 128 from 512 to the longest prefix, ties to the larger
+    # over multiples of 128 from 512 to the longest prefix, ties to the larger; then
+    # grown to cover whole contexts (<= 8192) when one partition holds each prefix
     if groups <= 0 or kvh <= 0 or max_prefix <= 0:
         return 512
     best, best_cost = None, None
@@ -74,24 +75,32 @@ def _shared_rule(groups, kvh, max_prefix, sms=152):
         cost = -(-items // sms) * (-(-min(part, max_prefix) // 128) + 1.4)
         if best is None or cost <= best_cost:
             best, best_cost = part, cost
+    whole = -(-max_ctx // 128) * 128
+    if best >= max_prefix and best < whole <= 8192 and num_seqs * kvh >= 2 * sms:
+        best = whole
     return best
 
 
 def test_automatic_shared_partition_size(pa):
-    # the forked-sampling batch: 32 prompts of 992 shared tokens, 8 kv heads -> one
-    # partition per (group, kv head)
-    assert pa.decode_shared_partition_size(32, 8, 992) == 1024
-    assert pa.decode_shared_partition_size(0, 8, 992) == 512           # no groups
-    assert pa.decode_shared_partition_size(32, 8, 0) == 512            # nothing shared
-    assert pa.decode_shared_partition_size(32, 8, 992, 256) == 256     # explicit sizes pass through
-    assert pa.decode_shared_partition_size(32, 8, 300) == 512          # never below 512
-    for groups, kvh, prefix in [(1, 8, 32768), (32, 8, 32768), (4, 1, 5000), (200, 8, 4096), (3, 2, 100000)]:
-        got = pa.decode_shared_partition_size(groups, kvh, prefix)
-        assert got == _shared_rule(groups, kvh, prefix), (groups, kvh, prefix, got)
+    # the forked-sampling batch: 256 sequences in 32 groups of 8, 992 shared tokens,
+    # contexts up to 1257 tokens, 8 kv heads -> one partition per group and kv head,
+    # grown to cover whole contexts (1280: no merge)
+    assert pa.decode_shared_partition_size(256, 32, 8, 992, 1257) == 1280
+    assert pa.decode_shared_partition_size(64, 8, 8, 992, 1257) == 512      # 8 groups: two partitions each
+    assert pa.decode_shared_partition_size(32, 4, 8, 992, 1257) == 512      # too few private items to grow
+    assert pa.decode_shared_partition_size(256, 0, 8, 992, 1257) == 512     # no groups
+    assert pa.decode_shared_partition_size(256, 32, 8, 0, 1257) == 512      # nothing shared
+    assert pa.decode_shared_partition_size(256, 32, 8, 992, 1257, 256) == 256   # explicit sizes pass through
+    assert pa.decode_shared_partition_size(256, 32, 8, 300, 1257) == 1280   # never below 512; grown
+    assert pa.decode_shared_partition_size(256, 32, 8, 992, 20000) == 1024  # contexts too long to cover
+    for args in [(8, 1, 8, 32768, 40000), (256, 32, 8, 32768, 33000), (20, 4, 1, 5000, 6000),
+                 (1600, 200, 8, 4096, 4500), (6, 3, 2, 100000, 100100), (512, 64, 8, 2000, 8192)]:
+        got = pa.decode_shared_partition_size(*args)
+        assert got == _shared_rule(*args), (args, got)
         assert got % 128 == 0 and got >= 512
         # the workspace sized for the automatic choice (0) covers it
-        assert pa.decode_shared_workspace_bytes(64, 32, 128, prefix + 4096, 0) >= \
-            pa.decode_shared_workspace_bytes(64, 32, 128, prefix + 4096, got)
+        assert pa.decode_shared_workspace_bytes(64, 32, 128, args[4], 0) >= \
+            pa.decode_shared_workspace_bytes(64, 32, 128, args[4], got)
 
 
 def test_status_strings(pa):

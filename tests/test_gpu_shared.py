@@ -81,16 +81,18 @@ def test_shared_prefix_sampling_reads_prompts_once(pa):
     assert_close(b[seqs], ref, "bf16", "shared-prefix decode")
 
 
-@pytest.mark.parametrize("partition", [0, 896, 2048])
+@pytest.mark.parametrize("partition", [0, 896, 1024, 2048])
 def test_shared_prefix_batch_partition_sizes(pa, partition):
     """The bench's forked-sampling batch (32 prompts x 8 samples): the automatic
-    partition (one per group and kv head, 1024 tokens) and explicit sizes that split
-    the 992 shared tokens unevenly (896 + 96) or cover shared and private tokens
-    alike (2048)."""
+    partition (1280 tokens: one per group and kv head, covering whole contexts, so
+    the per-sequence pass joins the shared partials and no merge runs), and explicit
+    sizes that split the 992 shared tokens unevenly (896 + 96), keep the merge (1024)
+    or cover shared and private tokens alike (2048)."""
     sc, w = _shared_prefix_state(num_prompts=32)
     pl, gm = pa.prefix_groups(w.block_tables, w.context_lens, w.block_size, 8)
     if partition == 0:
-        assert pa.decode_shared_partition_size(gm.shape[0], w.num_kv_heads, int(pl.max())) == 1024
+        assert pa.decode_shared_partition_size(w.num_seqs, gm.shape[0], w.num_kv_heads, int(pl.max()),
+                                               int(w.block_tables.shape[1]) * w.block_size) == 1280
     plain, shared, pl, gm = _run(pa, w, max_members=8, partition_size=partition)
     assert pa.get_device_error() == 0
     b = to_f64(shared)
@@ -99,6 +101,24 @@ def test_shared_prefix_batch_partition_sizes(pa, partition):
     seqs = np.arange(1, w.num_seqs, 5)
     w.slot_mapping = np.full(w.num_seqs, -1, np.int32)             # contents already complete
     assert_close(b[seqs], _oracle_full(w, seqs), "bf16", f"shared-prefix batch, partition {partition}")
+
+
+@pytest.mark.parametrize("G,dtype", [(4, "bf16"), (8, "f16"), (1, "bf16")])
+def test_whole_context_partition_joins_shared_partials(pa, G, dtype):
+    """A partition covering every whole context: the per-sequence pass joins the shared
+    pass's partials and writes the final rows itself (no merge). Groups whose members
+    have no private tokens at all (whole context shared: an item with no tiles that
+    only joins), members with one private token, and single sequences without a
+    group."""
+    groups = [(3, 5, 40), (4, 12, 0), (6, 20, 1), (2, 7, 300), (5, 3, 0)]
+    w = workloads.make_shared_groups(91 + G, groups, 4, 8 * G, 8, 128, 16, dtype)
+    mb = int(w.block_tables.shape[1]) * w.block_size
+    plain, shared, pl, gm = _run(pa, w, 8, partition_size=(mb + 127) // 128 * 128)
+    assert pa.get_device_error() == 0
+    assert np.any((pl > 0) & (pl == w.context_lens))                  # some contexts wholly shared
+    b = to_f64(shared)
+    assert np.abs(to_f64(plain) - b).max() <= 2e-2
+    assert_close(b, _oracle_full(w, np.arange(w.num_seqs)), dtype, f"whole-context partition G{G}")
 
 
 def _oracle_full(w, seqs):
