@@ -103,13 +103,13 @@ def test_shared_prefix_batch_partition_sizes(pa, partition):
     assert_close(b[seqs], _oracle_full(w, seqs), "bf16", f"shared-prefix batch, partition {partition}")
 
 
-@pytest.mark.parametrize("G,dtype", [(4, "bf16"), (8, "f16"), (1, "bf16")])
+@pytest.mark.parametrize("G,dtype", [(4, "bf16"), (8, "f16"), (1, "bf16"), (16, "bf16")])
 def test_whole_context_partition_joins_shared_partials(pa, G, dtype):
     """A partition covering every whole context: the per-sequence pass joins the shared
-    pass's partials and writes the final rows itself (no merge). Groups whose members
-    have no private tokens at all (whole context shared: an item with no tiles that
-    only joins), members with one private token, and single sequences without a
-    group."""
+    pass's partials and writes the final rows itself (no merge; at G = 16 the merge
+    still runs). Groups whose members have no private tokens at all (whole context
+    shared: an item with no tiles that only joins), members with one private token,
+    and single sequences without a group."""
     groups = [(3, 5, 40), (4, 12, 0), (6, 20, 1), (2, 7, 300), (5, 3, 0)]
     w = workloads.make_shared_groups(91 + G, groups, 4, 8 * G, 8, 128, 16, dtype)
     mb = int(w.block_tables.shape[1]) * w.block_size
