@@ -43,7 +43,10 @@
 //             warpgroup), and o = o * alpha + O_tile in registers.
 // Work items = (sequence, partition, kv head), dealt to CTAs in serpentine
 // rounds in order of decreasing size, from a bucketed prefix sum that each CTA
-// builds in shared memory at kernel start (decode_order.cuh). Every wait is bounded (see
+// builds in shared memory at kernel start (decode_order.cuh). The joining instance
+// (kFold) serves the sharing-aware decode when one partition covers every whole
+// context: each item loads its sequence's shared-prefix partial at item start and
+// writes the final row, so no merge runs. Every wait is bounded (see
 // sm100.cuh); on a timeout the kernel sets PA_DEVERR_WAIT, drains its copies and
 // returns.
 #include <cuda.h>
