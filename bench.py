@@ -551,7 +551,9 @@ def run_prefill(args, device, rank, world):
     ms = max_over_ranks(t0.elapsed_time(t1), device) / args.steps
     kern_ms, ncalls = time_calls(torch, st.prefill)
     peaks = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    # the kernel is timed alone, in short runs (clocks stay at their maximum), so the
+    # denominator is the burst GEMM figure, not the power-capped sustained one
+    peak = float(peaks.get("bf16_tflops", 1900.0))
     achieved = st.flops / (kern_ms * 1e-3) / 1e12
     frac, why = checked_roofline(achieved, peak, kern_ms, ms)
     line = {"metric": "paged chunked-prefill attention TFLOP/s on 1×GB300 (causal, packed chunks)",
@@ -560,7 +562,7 @@ def run_prefill(args, device, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": st.w.dtype, "data": "synthetic",
             "config": st.config(), "tokens_per_s": world * st.pw.total_q / (ms * 1e-3),
             "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
-                         "peak_kind": "measured bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks
+                         "peak_kind": "measured bf16_tflops (burst)" if "bf16_tflops" in peaks
                          else "fallback", "unit": "TFLOP/s", "frac": frac,
                          "algorithmic_flops_per_launch": st.flops, "kernel_ms": kern_ms,
                          "timed_launches": ncalls,
