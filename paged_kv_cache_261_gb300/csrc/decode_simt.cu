@@ -350,7 +350,11 @@ __device__ __forceinline__ void merge_row(const DecodeParams &p, int b, int h, i
 // (sequence, head) row, with no shared memory and no block barrier.
 constexpr int kWarpRowMaxParts = 32;
 
-template <typename T, int VEC>
+// kPre > 0 (launches whose rows hold at most kPre partitions): the partials go out
+// with the (m, l) pairs, so a row is one round trip; their slots are read even for
+// rows the partition kernel wrote itself, so launches where many rows are whole
+// (more partitions per row than kPre) keep the two round trips.
+template <typename T, int VEC, int kPre>
 __device__ __forceinline__ void merge_row_warp(const DecodeParams &p, int b, int h) {
     const int lane = threadIdx.x & 31;
     const int D = p.head_dim, P = p.max_partitions;
@@ -361,6 +365,26 @@ __device__ __forceinline__ void merge_row_warp(const DecodeParams &p, int b, int
     // is known: rows written directly by the partition kernel read none.
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + row0;
     float2 mine = lane < P ? ml[lane] : make_float2(-INFINITY, 0.f);
+    // the first kPre partials go out with them (slots past the row's count are read
+    // but never used)
+    const float *o = p.ws_o + row0 * D + lane * VEC;
+    float pre[kPre > 0 ? kPre : 1][VEC];
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+        if (i < P) {
+            if constexpr (VEC == 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(o + (int64_t)i * D);
+                pre[i][0] = x.x;
+                pre[i][1] = x.y;
+                pre[i][2] = x.z;
+                pre[i][3] = x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2 *>(o + (int64_t)i * D);
+                pre[i][0] = x.x;
+                pre[i][1] = x.y;
+            }
+        }
+    }
     const SeqSplit sp = seq_split(p, b);
     if (sp.direct) return;                      // the partition kernel wrote the row
     const int nparts = sp.shared + sp.priv;
@@ -376,9 +400,16 @@ __device__ __forceinline__ void merge_row_warp(const DecodeParams &p, int b, int
     float acc[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-    const float *o = p.ws_o + row0 * D + lane * VEC;
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+        const float c = __shfl_sync(0xffffffffu, c_mine, i);
+        if (i < nparts) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc[v] = fmaf(c, pre[i][v], acc[v]);
+        }
+    }
 #pragma unroll 4
-    for (int i = 0; i < nparts; ++i) {
+    for (int i = kPre; i < nparts; ++i) {
         const float c = __shfl_sync(0xffffffffu, c_mine, i);
         if constexpr (VEC == 4) {
             const float4 x = *reinterpret_cast<const float4 *>(o + (int64_t)i * D);
@@ -397,14 +428,14 @@ __device__ __forceinline__ void merge_row_warp(const DecodeParams &p, int b, int
     for (int v = 0; v < VEC; ++v) dst[v] = Elem<T>::from_f(acc[v]);
 }
 
-template <typename T>
+template <typename T, int kPre>
 __global__ __launch_bounds__(kReduceThreads) void decode_reduce_warp_kernel(const DecodeParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t row = (int64_t)blockIdx.x * kReduceWarps + (threadIdx.x >> 5);
     if (row >= (int64_t)p.num_seqs * p.num_heads) return;
     const int b = (int)(row / p.num_heads), h = (int)(row % p.num_heads);
-    if (p.head_dim == 128) merge_row_warp<T, 4>(p, b, h);
-    else merge_row_warp<T, 2>(p, b, h);
+    if (p.head_dim == 128) merge_row_warp<T, 4, kPre>(p, b, h);
+    else merge_row_warp<T, 2, kPre>(p, b, h);
 }
 
 template <typename T>
@@ -469,9 +500,14 @@ int launch_decode_simt(const DecodeParams &p, int dtype, cudaStream_t stream) {
 template <typename T>
 int launch_reduce_t(const DecodeParams &p, cudaStream_t stream) {
     if (p.max_partitions <= kWarpRowMaxParts) {
+        // rows of at most 4 partitions: their partials are loaded with the (m, l) pairs
+        // (8B-shaped batch: 0.0974 -> 0.0965 ms a call; with up to 8 partitions, most rows
+        // of the mixed-serving batch are whole and the early loads cost more than they save)
         const int64_t rows = (int64_t)p.num_seqs * p.num_heads;
         dim3 grid((unsigned)((rows + kReduceWarps - 1) / kReduceWarps));
-        return launch_pdl(decode_reduce_warp_kernel<T>, grid, dim3(kReduceThreads), 0, stream, p);
+        if (p.max_partitions <= 4)
+            return launch_pdl(decode_reduce_warp_kernel<T, 4>, grid, dim3(kReduceThreads), 0, stream, p);
+        return launch_pdl(decode_reduce_warp_kernel<T, 0>, grid, dim3(kReduceThreads), 0, stream, p);
     }
     // Launched plainly: measured on the long-context batch, early-launched CTAs of
     // this form slowed the partition kernel down (0.4608 vs 0.4515 ms).
