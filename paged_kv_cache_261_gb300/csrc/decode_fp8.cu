@@ -346,10 +346,11 @@ __global__ __launch_bounds__(kThreads, ctas_per_sm(GT)) void decode_fp8_kernel(c
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    // Programmatic dependent launch: only barrier set-up and the tensor-memory
-    // allocation above overlap the preceding kernel.
+    // Programmatic dependent launch: the set-up above and the item order below,
+    // which reads only the call's lengths, overlap the preceding kernel (the previous
+    // call's merge, or the 8-bit scatter, which writes cache rows); everything after
+    // the wait may touch what that kernel reads or writes.
     asm volatile("griddepcontrol.launch_dependents;");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     int *order = reinterpret_cast<int *>(smem + kOffOrder);
     int *counts = reinterpret_cast<int *>(smem + kOffMisc + 8);   // [0] = n4, [1] = list length
@@ -372,6 +373,7 @@ __global__ __launch_bounds__(kThreads, ctas_per_sm(GT)) void decode_fp8_kernel(c
         reinterpret_cast<uint4 *>(sP)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0 || warp == kVProdWarp) {
         // ------------------------------------------------------------ producers

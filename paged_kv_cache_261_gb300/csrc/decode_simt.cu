@@ -430,6 +430,9 @@ __device__ __forceinline__ void merge_row_warp(const DecodeParams &p, int b, int
 
 template <typename T, int kPre>
 __global__ __launch_bounds__(kReduceThreads) void decode_reduce_warp_kernel(const DecodeParams p) {
+    // the next call's partition kernel may launch and set itself up meanwhile (it
+    // waits for this grid before it touches the workspace or the output)
+    asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t row = (int64_t)blockIdx.x * kReduceWarps + (threadIdx.x >> 5);
     if (row >= (int64_t)p.num_seqs * p.num_heads) return;

@@ -253,10 +253,11 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         tmem_relinquish();
     }
     // Programmatic dependent launch: the merge kernel may launch now (it waits for
-    // this grid to finish). Only barrier set-up and the tensor-memory allocation
-    // above overlap the preceding kernel; everything below may read what it wrote.
+    // this grid to finish). The set-up above and the item order below, which reads
+    // only the call's lengths, overlap the preceding kernel (the previous call's
+    // merge, which writes only output rows); everything after the wait may touch
+    // what that kernel reads or writes.
     asm volatile("griddepcontrol.launch_dependents;");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Item order (see decode_order.cuh); the byte codes use the P buffer, which is
     // unused until the first tile.
@@ -275,6 +276,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     decode_order::build_item_table<(decode_order::kTableItems + kThreads - 1) / kThreads>(p, prefix, order, n4, cache, total_items, items);
     const int nmy = decode_order::cta_items(total_items);
     __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0 || warp == kVProdWarp) {
         // ------------------------------------------------------------ producers
