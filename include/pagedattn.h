@@ -35,6 +35,13 @@
  * device (a bad slot, block id, copy pair or context length) skip the bad
  * access and set a bit in a per-device error word, read and cleared by
  * pa_get_device_error(). No kernel traps or asserts.
+ *
+ * Launch chaining: the decode and merge kernels are launched as programmatic
+ * dependents of the kernel before them on the stream, and the decode kernels read
+ * context_lens (and prefix_lens) before they wait for it. A kernel the caller
+ * launches just before a decode call therefore must not write those two arrays
+ * after it signals its dependents early (griddepcontrol.launch_dependents); a
+ * kernel that never signals is waited for in full, as usual.
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H
