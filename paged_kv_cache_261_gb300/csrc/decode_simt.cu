@@ -443,6 +443,8 @@ __global__ __launch_bounds__(kReduceThreads) void decode_reduce_warp_kernel(cons
 
 template <typename T>
 __global__ __launch_bounds__(kReduceThreads) void decode_reduce_kernel(const DecodeParams p) {
+    // the next call's partition kernel may launch and set itself up meanwhile
+    asm volatile("griddepcontrol.launch_dependents;");
     // a no-op unless launched as a programmatic dependent of the partition kernel
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ __align__(16) float part_sum[kReduceWarps * 128];

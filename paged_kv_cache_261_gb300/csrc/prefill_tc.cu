@@ -175,6 +175,9 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    // a decode launched after this kernel (the sharing-aware decode's per-sequence
+    // pass) may set itself up now; it waits for this grid before reading its partials
+    asm volatile("griddepcontrol.launch_dependents;");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
