@@ -334,10 +334,12 @@ int pa_paged_attention_decode(void *out, const void *q, const void *key_cache,
 
     const DecodeKernel choice = decode_kernel_choice();
     int krc;
-    if (choice == DecodeKernel::Tc || (choice == DecodeKernel::Auto && pa::decode_tc_supported(p, dtype)))
+    if (choice == DecodeKernel::Tc || (choice == DecodeKernel::Auto && pa::decode_tc_supported(p, dtype))) {
         krc = pa::launch_decode_tc(p, dtype, s);
-    else
+        p.chain_next = 1;
+    } else {
         krc = pa::launch_decode_simt(p, dtype, s);
+    }
     if (krc == 0 && P > 1) krc = pa::launch_decode_reduce(p, dtype, s);
     if (owned) cudaFreeAsync(owned, s);
     if (krc == -2) return PA_ERR_UNSUPPORTED;
@@ -374,6 +376,7 @@ int pa_paged_attention_decode_append(void *out, const void *q, const void *k_new
         p.app_v = v_new;
         p.app_slots = slot_mapping;
         krc = pa::launch_decode_tc(p, dtype, s);
+        p.chain_next = 1;
     } else {
         // the scatter, then the decode (head_dim 64 or 128 keeps a row a multiple of
         // the scatter's 16-byte copies)
@@ -584,6 +587,7 @@ int pa_paged_attention_decode_shared(void *out, const void *q, const void *key_c
     int rc = 0;
     if (num_groups > 0 && g.shared_parts > 0) rc = pa::launch_shared_prefix_tc(g, dtype, s);
     if (rc == 0) rc = pa::launch_decode_tc(d, dtype, s);
+    d.chain_next = 1;
     if (rc == 0 && !d.fold_shared) rc = pa::launch_decode_reduce(d, dtype, s);
     if (owned) cudaFreeAsync(ws, s);
     if (rc == -2) return PA_ERR_UNSUPPORTED;

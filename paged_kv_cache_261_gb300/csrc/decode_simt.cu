@@ -430,9 +430,9 @@ __device__ __forceinline__ void merge_row_warp(const DecodeParams &p, int b, int
 
 template <typename T, int kPre>
 __global__ __launch_bounds__(kReduceThreads) void decode_reduce_warp_kernel(const DecodeParams p) {
-    // the next call's partition kernel may launch and set itself up meanwhile (it
-    // waits for this grid before it touches the workspace or the output)
-    asm volatile("griddepcontrol.launch_dependents;");
+    // chain_next: the next call's partition kernel may launch and set itself up
+    // meanwhile (it waits for this grid before it touches the workspace or the output)
+    if (p.chain_next) asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t row = (int64_t)blockIdx.x * kReduceWarps + (threadIdx.x >> 5);
     if (row >= (int64_t)p.num_seqs * p.num_heads) return;
@@ -443,8 +443,6 @@ __global__ __launch_bounds__(kReduceThreads) void decode_reduce_warp_kernel(cons
 
 template <typename T>
 __global__ __launch_bounds__(kReduceThreads) void decode_reduce_kernel(const DecodeParams p) {
-    // the next call's partition kernel may launch and set itself up meanwhile
-    asm volatile("griddepcontrol.launch_dependents;");
     // a no-op unless launched as a programmatic dependent of the partition kernel
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ __align__(16) float part_sum[kReduceWarps * 128];

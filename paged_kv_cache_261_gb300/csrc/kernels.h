@@ -45,6 +45,11 @@ struct DecodeParams {
     // partial (slot 0) with its own and writes the final row, so no merge runs; a
     // sequence whose whole context is shared gets an item with no tiles that only joins.
     int fold_shared;
+    // Set with the tensor-core partition kernel: the one-warp-per-row merge lets the
+    // next launch on the stream (the next call's partition kernel) start its set-up
+    // while it runs. Not with the 8-bit kernel, whose two CTAs per SM, resident
+    // early, slow that merge down more than their set-up gains.
+    int chain_next;
 };
 
 // Chunked prefill: every query row of a packed chunk attends causally.
