@@ -41,9 +41,17 @@ def _variants(w, n, seed):
     return out
 
 
+@pytest.mark.parametrize("long", [False, True], ids=["warp_merge", "block_merge"])
 @pytest.mark.parametrize("fp8", [False, True])
-def test_back_to_back_calls_equal_isolated_calls(pa, fp8):
-    ctx = np.random.default_rng(11).integers(300, 4096, size=48).astype(np.int32)
+def test_back_to_back_calls_equal_isolated_calls(pa, fp8, long):
+    """block_merge: few sequences of 17k-40k tokens in partitions of 512, so rows hold
+    up to 79 partitions and the merge of one CTA per row follows the partition kernel."""
+    if long:
+        ctx = np.random.default_rng(13).integers(17000, 40000, size=4).astype(np.int32)
+        part = 512
+    else:
+        ctx = np.random.default_rng(11).integers(300, 4096, size=48).astype(np.int32)
+        part = 0
     w = workloads.make_decode("chain", 811, ctx, 32, 8, 128, 16, "bf16")
     d = dev()
     shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
@@ -58,14 +66,16 @@ def test_back_to_back_calls_equal_isolated_calls(pa, fp8):
     bt = torch.as_tensor(w.block_tables, device=d)
     lens = _variants(w, 6, 12 + int(fp8))
     mc = int(w.context_lens.max())
-    ws = torch.empty(pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, mc, 0), dtype=torch.uint8,
+    ws = torch.empty(pa.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, mc, part), dtype=torch.uint8,
                      device=d)
 
     def call(out, cl):
         if fp8:
-            pa.paged_attention_decode_fp8(out, q, kc, vc, bt, cl, w.scale, S, S, max_context_len=mc, workspace=ws)
+            pa.paged_attention_decode_fp8(out, q, kc, vc, bt, cl, w.scale, S, S, max_context_len=mc,
+                                          partition_size=part, workspace=ws)
         else:
-            pa.paged_attention_decode(out, q, kc, vc, bt, cl, w.scale, max_context_len=mc, workspace=ws)
+            pa.paged_attention_decode(out, q, kc, vc, bt, cl, w.scale, max_context_len=mc, partition_size=part,
+                                      workspace=ws)
 
     alone = []
     for cl in lens:
