@@ -392,6 +392,26 @@ def test_decode_kernels_against_oracle(pa, force_kernel, kernel, bs, dtype, H, H
     _errors_clear(pa)
 
 
+@pytest.mark.parametrize("H", [64, 32])
+def test_tc_many_short_items_per_cta(pa, force_kernel, H):
+    """About thirty items per CTA, most of one or two tiles, empty contexts among them and
+    partitions of 256 splitting the longer ones: at G = 8 each item's finish is deferred
+    past the next item's first tile (at G = 4 it is not); every row against the oracle."""
+    force_kernel("tc")
+    rng = np.random.default_rng(47 + H)
+    ctx = rng.integers(1, 700, size=600).astype(np.int32)
+    ctx[::7] = 0
+    ctx[5::11] = 1
+    w = workloads.make_decode(f"short_items_{H}", 47, ctx, H, 8, 128, 16, "bf16")
+    out, kc, vc = gpu_decode(w, max_context_len=int(ctx.max()), partition_size=256)
+    check_newest_rows(w, kc, vc)
+    seqs = np.concatenate([np.arange(0, 600, 13), [1, 5, 6, 7, 16, 597, 598, 599]])
+    got = to_f64(out)
+    assert np.all(got[ctx == 0] == 0.0)
+    assert_close(got[seqs], oracle_decode(w, seqs), "bf16", f"short items H{H}")
+    _errors_clear(pa)
+
+
 def test_tc_kernel_bad_block_id_reads_zeros(pa, force_kernel):
     force_kernel("tc")
     w = workloads.make_decode("badid_tc", 3, np.array([300, 300], np.int32), 8, 2, 128, 16, "bf16")
