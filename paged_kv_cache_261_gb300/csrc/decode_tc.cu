@@ -40,7 +40,10 @@
 //             scale, mask, tile max through shuffles + shared memory, exp2,
 //             P^T to shared memory (bf16/f16, 128-byte swizzled K-major), zero
 //             V rows of masked tokens (their contents may be anything; the first
-//             warpgroup), and o = o * alpha + O_tile in registers.
+//             warpgroup), and o = o * alpha + O_tile in registers. In the G = 8 and
+//             joining instances an item's finish (its last O, the sum of l over
+//             the warps, the output) waits until the next item's first tile has
+//             been through the softmax, so no warpgroup idles at item boundaries.
 // Work items = (sequence, partition, kv head), dealt to CTAs in serpentine
 // rounds in order of decreasing size, from a bucketed prefix sum that each CTA
 // builds in shared memory at kernel start (decode_order.cuh). The joining instance
