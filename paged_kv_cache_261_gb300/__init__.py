@@ -148,6 +148,12 @@ def _storage_code(t) -> int:
     return PA_DTYPE_E4M3 if _is_fp8_cache(t) else _dtype_code(t)
 
 
+def _on(device):
+    """The tensors' device made current for a library call: the library launches on,
+    and sizes its grids for, the current device."""
+    return _torch().cuda.device(device)
+
+
 def _stream_ptr(stream, device) -> int:
     torch = _torch()
     if stream is None:
@@ -182,9 +188,10 @@ def paged_kv_write(k, v, slot_mapping, key_cache, value_cache, stream=None) -> N
     T = slot_mapping.shape[0]
     if tuple(k.shape) != (T, hk, d) or tuple(v.shape) != (T, hk, d):
         raise ValueError(f"k/v must be [{T}, {hk}, {d}]")
-    rc = _lib.pa_paged_kv_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
-                                key_cache.data_ptr(), value_cache.data_ptr(), nb, bs, hk, d,
-                                _dtype_code(key_cache), _stream_ptr(stream, dev))
+    with _on(dev):
+        rc = _lib.pa_paged_kv_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                                    key_cache.data_ptr(), value_cache.data_ptr(), nb, bs, hk, d,
+                                    _dtype_code(key_cache), _stream_ptr(stream, dev))
     _check(rc, "pa_paged_kv_write")
 
 
@@ -259,11 +266,12 @@ def paged_attention_decode(out, q, key_cache, value_cache, block_tables, context
             workspace = _workspace(dev, sp, need)
         _cuda(workspace, "workspace", torch.uint8, dev)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
-    rc = _lib.pa_paged_attention_decode(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
-                                        value_cache.data_ptr(), block_tables.data_ptr(), mb,
-                                        context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
-                                        int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
-                                        _dtype_code(key_cache), sp)
+    with _on(dev):
+        rc = _lib.pa_paged_attention_decode(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
+                                            value_cache.data_ptr(), block_tables.data_ptr(), mb,
+                                            context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
+                                            int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
+                                            _dtype_code(key_cache), sp)
     _check(rc, "pa_paged_attention_decode")
 
 
@@ -305,12 +313,13 @@ def paged_attention_decode_append(out, q, k_new, v_new, slot_mapping, key_cache,
             workspace = _workspace(dev, sp, need)
         _cuda(workspace, "workspace", torch.uint8, dev)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
-    rc = _lib.pa_paged_attention_decode_append(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
-                                               slot_mapping.data_ptr(), key_cache.data_ptr(),
-                                               value_cache.data_ptr(), block_tables.data_ptr(), mb,
-                                               context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
-                                               int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
-                                               _dtype_code(key_cache), sp)
+    with _on(dev):
+        rc = _lib.pa_paged_attention_decode_append(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                                   slot_mapping.data_ptr(), key_cache.data_ptr(),
+                                                   value_cache.data_ptr(), block_tables.data_ptr(), mb,
+                                                   context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
+                                                   int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
+                                                   _dtype_code(key_cache), sp)
     _check(rc, "pa_paged_attention_decode_append")
 
 
@@ -337,11 +346,12 @@ def paged_attention_prefill(out, q, key_cache, value_cache, block_tables, contex
         raise ValueError("q/out must be [T, H, head_dim]")
     if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(query_start_loc.shape) != (B + 1,):
         raise ValueError("block_tables must be [B, MB] and query_start_loc [B + 1]")
-    rc = _lib.pa_paged_attention_prefill(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
-                                         value_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
-                                         context_lens.data_ptr(), query_start_loc.data_ptr(), B, T,
-                                         int(max_query_len), H, hk, D, bs, nb, float(scale),
-                                         _dtype_code(key_cache), _stream_ptr(stream, dev))
+    with _on(dev):
+        rc = _lib.pa_paged_attention_prefill(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
+                                             value_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+                                             context_lens.data_ptr(), query_start_loc.data_ptr(), B, T,
+                                             int(max_query_len), H, hk, D, bs, nb, float(scale),
+                                             _dtype_code(key_cache), _stream_ptr(stream, dev))
     _check(rc, "pa_paged_attention_prefill")
 
 
@@ -400,13 +410,14 @@ def paged_attention_decode_shared(out, q, key_cache, value_cache, block_tables, 
         workspace = _workspace(dev, sp, need)
     _cuda(workspace, "workspace", torch.uint8, dev)
     ng, mm = group_members.shape
-    rc = _lib.pa_paged_attention_decode_shared(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
-                                               value_cache.data_ptr(), block_tables.data_ptr(), mb,
-                                               context_lens.data_ptr(), prefix_lens.data_ptr(),
-                                               group_members.data_ptr() if ng else None, ng, max(mm, 1), mpre,
-                                               B, H, hk, D, bs, nb, float(scale), int(max_context_len),
-                                               int(partition_size), workspace.data_ptr(), workspace.numel(),
-                                               _dtype_code(key_cache), sp)
+    with _on(dev):
+        rc = _lib.pa_paged_attention_decode_shared(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
+                                                   value_cache.data_ptr(), block_tables.data_ptr(), mb,
+                                                   context_lens.data_ptr(), prefix_lens.data_ptr(),
+                                                   group_members.data_ptr() if ng else None, ng, max(mm, 1), mpre,
+                                                   B, H, hk, D, bs, nb, float(scale), int(max_context_len),
+                                                   int(partition_size), workspace.data_ptr(), workspace.numel(),
+                                                   _dtype_code(key_cache), sp)
     _check(rc, "pa_paged_attention_decode_shared")
 
 
@@ -420,9 +431,10 @@ def copy_blocks(key_cache, value_cache, src_dst_pairs, stream=None) -> None:
     if src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
         raise ValueError("src_dst_pairs must be [P, 2]")
     nb, bs, hk, d = key_cache.shape
-    rc = _lib.pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr(), src_dst_pairs.data_ptr(),
-                             src_dst_pairs.shape[0], nb, bs, hk, d, _storage_code(key_cache),
-                             _stream_ptr(stream, dev))
+    with _on(dev):
+        rc = _lib.pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr(), src_dst_pairs.data_ptr(),
+                                 src_dst_pairs.shape[0], nb, bs, hk, d, _storage_code(key_cache),
+                                 _stream_ptr(stream, dev))
     _check(rc, "pa_copy_blocks")
 
 
@@ -449,9 +461,10 @@ def paged_kv_write_fp8(k, v, slot_mapping, key_cache, value_cache, k_scale: floa
     T = slot_mapping.shape[0]
     if tuple(k.shape) != (T, hk, d) or tuple(v.shape) != (T, hk, d):
         raise ValueError(f"k/v must be [{T}, {hk}, {d}]")
-    rc = _lib.pa_paged_kv_write_fp8(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T, key_cache.data_ptr(),
-                                    value_cache.data_ptr(), nb, bs, hk, d, float(k_scale), float(v_scale),
-                                    _dtype_code(k), _stream_ptr(stream, dev))
+    with _on(dev):
+        rc = _lib.pa_paged_kv_write_fp8(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T, key_cache.data_ptr(),
+                                        value_cache.data_ptr(), nb, bs, hk, d, float(k_scale), float(v_scale),
+                                        _dtype_code(k), _stream_ptr(stream, dev))
     _check(rc, "pa_paged_kv_write_fp8")
 
 
@@ -482,11 +495,12 @@ def paged_attention_decode_fp8(out, q, key_cache, value_cache, block_tables, con
             workspace = _workspace(dev, sp, need)
         _cuda(workspace, "workspace", torch.uint8, dev)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
-    rc = _lib.pa_paged_attention_decode_fp8(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
-                                            value_cache.data_ptr(), block_tables.data_ptr(), mb,
-                                            context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
-                                            float(k_scale), float(v_scale), int(max_context_len),
-                                            int(partition_size), ws_ptr, ws_bytes, _dtype_code(q), sp)
+    with _on(dev):
+        rc = _lib.pa_paged_attention_decode_fp8(out.data_ptr(), q.data_ptr(), key_cache.data_ptr(),
+                                                value_cache.data_ptr(), block_tables.data_ptr(), mb,
+                                                context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
+                                                float(k_scale), float(v_scale), int(max_context_len),
+                                                int(partition_size), ws_ptr, ws_bytes, _dtype_code(q), sp)
     _check(rc, "pa_paged_attention_decode_fp8")
 
 
@@ -525,12 +539,13 @@ def paged_attention_decode_fp8_append(out, q, k_new, v_new, slot_mapping, key_ca
             workspace = _workspace(dev, sp, need)
         _cuda(workspace, "workspace", torch.uint8, dev)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
-    rc = _lib.pa_paged_attention_decode_fp8_append(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
-                                                   slot_mapping.data_ptr(), key_cache.data_ptr(),
-                                                   value_cache.data_ptr(), block_tables.data_ptr(), mb,
-                                                   context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
-                                                   float(k_scale), float(v_scale), int(max_context_len),
-                                                   int(partition_size), ws_ptr, ws_bytes, _dtype_code(q), sp)
+    with _on(dev):
+        rc = _lib.pa_paged_attention_decode_fp8_append(out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                                       slot_mapping.data_ptr(), key_cache.data_ptr(),
+                                                       value_cache.data_ptr(), block_tables.data_ptr(), mb,
+                                                       context_lens.data_ptr(), B, H, hk, D, bs, nb, float(scale),
+                                                       float(k_scale), float(v_scale), int(max_context_len),
+                                                       int(partition_size), ws_ptr, ws_bytes, _dtype_code(q), sp)
     _check(rc, "pa_paged_attention_decode_fp8_append")
 
 
@@ -539,7 +554,8 @@ def get_device_error(stream=None, device=None) -> int:
     torch = _torch()
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     bits = ctypes.c_uint32(0)
-    rc = _lib.pa_get_device_error(_stream_ptr(stream, dev), ctypes.byref(bits))
+    with _on(dev):
+        rc = _lib.pa_get_device_error(_stream_ptr(stream, dev), ctypes.byref(bits))
     if rc not in (PA_OK, PA_ERR_DEVICE_INDEX):
         raise PagedAttnError(rc, "pa_get_device_error")
     return int(bits.value)
@@ -558,7 +574,8 @@ def check_bounded_wait(limit_ns: int, report=None, stream=None) -> None:
             raise ValueError("report needs 4 int64 elements")
         dev = report.device
         ptr = report.data_ptr()
-    _check(_lib.pa_check_bounded_wait(int(limit_ns), ptr, _stream_ptr(stream, dev)), "pa_check_bounded_wait")
+    with _on(dev):
+        _check(_lib.pa_check_bounded_wait(int(limit_ns), ptr, _stream_ptr(stream, dev)), "pa_check_bounded_wait")
 
 
 from .allocator import AllocStats, BlockAllocator  # noqa: E402,F401
