@@ -60,10 +60,23 @@ _KERNEL_SOURCES = {
     "decode_fp8": ["decode_fp8.cu", "decode_order.cuh", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h",
                    "kernels_fp8.h", "fp8_encode.cuh"],
     "prefill_tc": ["prefill_tc.cu", "prefill_common.cuh", "sm100.cuh", "common.cuh", "tma_maps.cuh", "kernels.h"],
+    # the sharing-aware decode's two passes: group mode of the prefill kernel + the
+    # tensor-core decode (its record is the DRAM bytes of both launches of one call)
+    "shared_decode": ["prefill_tc.cu", "prefill_common.cuh", "decode_tc.cu", "decode_order.cuh", "sm100.cuh",
+                      "common.cuh", "tma_maps.cuh", "kernels.h"],
 }
 
 DECODE_WORKLOADS = ("llama8b_decode", "long_context", "mixed_serving")
 FP8_WORKLOADS = tuple(n + "_fp8" for n in DECODE_WORKLOADS)
+
+
+def traffic_family(workload: str) -> str:
+    """The kernel family whose sources key a workload's DRAM-traffic record."""
+    if workload == "chunked_prefill":
+        return "prefill_tc"
+    if workload == "shared_prefix":
+        return "shared_decode"
+    return "decode_fp8" if workload.endswith("_fp8") else "decode_tc"
 
 
 def base_workload(name: str):
@@ -568,7 +581,7 @@ def run_prefill(args, device, rank, world):
                          "timed_launches": ncalls,
                          "timing": f"median over {KERNEL_RUNS} event-bracketed runs of {KERNEL_CALLS} back-to-back "
                                    f"prefill calls, after the timed steps",
-                         "traffic": recorded_traffic("chunked_prefill", "prefill_tc")},
+                         "traffic": recorded_traffic("chunked_prefill", traffic_family("chunked_prefill"))},
             "gpu_launches": st.launches_per_step * args.steps, "clocks": clocks}
     if why:
         line["roofline"]["frac_null_reason"] = why
@@ -818,13 +831,15 @@ def decode_roofline(torch, st: "Step", device, peak: float, peak_kind: str, ms_s
     frac, why = checked_roofline(achieved, peak, kern_ms, ref_ms)
     kernel = (("decode call: decode_fp8_kernel (partitions; writes the new tokens) + merge" if st.append
                else "decode_fp8_kernel + merge") if st.fp8 else
-              "shared-prefix pass + private decode_tc_kernel pass + merge" if shared else
+              ("decode call: shared-prefix pass (prefill_tc_kernel, group mode) + private decode_tc_kernel pass "
+               "(joining the shared partials; a merge only when one partition does not cover every context)")
+              if shared else
               "decode call: decode_tc_kernel (partitions; writes the new tokens) + merge")
     roof = {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peak,
             "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": frac,
             "algorithmic_bytes_per_launch": bytes_, "decode_ms": kern_ms, "timed_launches": ncalls,
             "timing": timing, "decode_ms_bracketed_median": bracketed,
-            "traffic": recorded_traffic(st.name, "decode_fp8" if st.fp8 else "decode_tc")}
+            "traffic": recorded_traffic(st.name, traffic_family(st.name))}
     if shared:
         roof["logical_bytes_per_launch"] = st.decode_bytes
         roof["bytes"] = "unique: every shared prefix block counted once per group"

@@ -28,6 +28,7 @@ codes with one float32 scale for K and one for V.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -148,10 +149,17 @@ def _storage_code(t) -> int:
     return PA_DTYPE_E4M3 if _is_fp8_cache(t) else _dtype_code(t)
 
 
+_SAME_DEVICE = contextlib.nullcontext()
+
+
 def _on(device):
     """The tensors' device made current for a library call: the library launches on,
-    and sizes its grids for, the current device."""
-    return _torch().cuda.device(device)
+    and sizes its grids for, the current device (no switch when it already is)."""
+    torch = _torch()
+    idx = device.index
+    if idx is None or idx == torch.cuda.current_device():
+        return _SAME_DEVICE
+    return torch.cuda.device(idx)
 
 
 def _stream_ptr(stream, device) -> int:

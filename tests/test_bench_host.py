@@ -31,8 +31,7 @@ def test_every_traffic_record_names_a_kernel_family():
     for wl, ent in rec.items():
         assert ent["dram_bytes_per_launch"] > 0
         assert len(ent["source_digest"]) == 16
-        fam = "decode_fp8" if wl.endswith("_fp8") else ("prefill_tc" if wl == "chunked_prefill" else "decode_tc")
-        assert fam in bench._KERNEL_SOURCES
+        assert bench.traffic_family(wl) in bench._KERNEL_SOURCES
 
 
 def test_reference_arm_prints_the_contract_line(capsys):
