@@ -500,28 +500,28 @@ __global__ __launch_bounds__(kThreads, 1) void prefill_tc_kernel(const __grid_co
                     }
                     tmem_wait_st();
                 }
+                const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;    // rows with no visible key: p = 0
+                float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
+                // the weights in registers first (keys as 16-bit pairs), so they are computed
+                // while the previous tile's P.V runs; P is stored once that MMA has read it
+                uint32_t pw[64];
+#pragma unroll
+                for (int q = 0; q < 64; ++q) {
+                    const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1])),
+                                           sc2, nm2);
+                    const float2 pv = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                    pw[q] = pack2<T>(pv.x, pv.y);
+                    ls2[q & 1] = fadd2(ls2[q & 1], pv);
+                }
                 // P was last read by the MMA of tile it-1
                 if (it >= 1 && !warp_wait(&o_done[(it - 1) & 1], ((it - 1) >> 1) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;    // rows with no visible key: p = 0
-                float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pw[32];                  // keys 64h .. 64h + 63 as 16-bit pairs
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const float2 x = ffma2(make_float2(__uint_as_float(sr[h * 64 + 2 * q]),
-                                                           __uint_as_float(sr[h * 64 + 2 * q + 1])), sc2, nm2);
-                        const float2 pv = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                        pw[q] = pack2<T>(pv.x, pv.y);
-                        ls2[q & 1] = fadd2(ls2[q & 1], pv);
-                    }
-                    tmem_st32(tmem + lane_off + kColP + h * 32, pw);
-                }
+                tmem_st32(tmem + lane_off + kColP, pw);
+                tmem_st32(tmem + lane_off + kColP + 32, pw + 32);
                 tmem_wait_st();
                 l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
                 // key row r past every row's last visible key: its slot may hold anything
