@@ -283,10 +283,13 @@ __global__ __launch_bounds__(kThreads) void decode_simt_kernel(const DecodeParam
 
 // Merge of partition partials: M = max m_p, L = sum l_p 2^(m_p - M),
 // out = sum_p o_p 2^(m_p - M) / L. One CTA of 8 warps per (query head,
-// sequence): warp 0 finds M and L (lanes over partitions), then every warp
-// accumulates a strided subset of the partitions with each lane owning 4
-// (head_dim 128) or 2 (head_dim 64) consecutive dimensions, and the 8 warp sums
-// are added through shared memory.
+// sequence): every warp takes a strided subset of the partitions in one pass,
+// keeping its own running max, sum and output (each lane owning 4 (head_dim 128)
+// or 2 (head_dim 64) consecutive dimensions), and the 8 warps' results are
+// combined through shared memory. (A first pass of warp 0 over the (m, l) pairs
+// for M and L, with the other warps waiting, cost two round trips a row; a pass
+// that rescaled after every partition kept one partition's loads in flight per
+// warp and was slower still.)
 constexpr int kReduceWarps = 8;
 constexpr int kReduceThreads = 32 * kReduceWarps;
 
@@ -297,52 +300,76 @@ __device__ __forceinline__ void merge_row(const DecodeParams &p, int b, int h, i
     const int D = p.head_dim, P = p.max_partitions;
     const int64_t row0 = ((int64_t)b * p.num_heads + h) * P;
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + row0;
-    if (warp == 0) {
-        float m = -INFINITY;
-        for (int i = lane; i < nparts; i += 32) m = fmaxf(m, ml[i].x);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float l = 0.f;
-        for (int i = lane; i < nparts; i += 32) {
-            const float2 v = ml[i];
-            l += v.y * fast_exp2(v.x - m);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) {
-            ml_s[0] = m;
-            ml_s[1] = 1.f / l;
-        }
-    }
-    __syncthreads();
-    const float M = ml_s[0], inv = ml_s[1];
-    float acc[VEC];
+    const float *o = p.ws_o + row0 * D + lane * VEC;
+    // one pass: the warp's running max m, sum l and output over its partitions, loaded
+    // kBatch at a time (all loads of a batch in flight together) and rescaled once per
+    // batch to the batch's max
+    constexpr int kBatch = 8;
+    float m = -INFINITY, l = 0.f, acc[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-    const float *o = p.ws_o + row0 * D + lane * VEC;
-#pragma unroll 4
-    for (int i = warp; i < nparts; i += kReduceWarps) {
-        const float c = fast_exp2(ml[i].x - M) * inv;
-        if constexpr (VEC == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(o + (int64_t)i * D);
-            acc[0] = fmaf(c, x.x, acc[0]);
-            acc[1] = fmaf(c, x.y, acc[1]);
-            acc[2] = fmaf(c, x.z, acc[2]);
-            acc[3] = fmaf(c, x.w, acc[3]);
-        } else {
-            const float2 x = *reinterpret_cast<const float2 *>(o + (int64_t)i * D);
-            acc[0] = fmaf(c, x.x, acc[0]);
-            acc[1] = fmaf(c, x.y, acc[1]);
+    for (int i0 = warp; i0 < nparts; i0 += kReduceWarps * kBatch) {
+        float2 mi[kBatch];
+        float x[kBatch][VEC];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int i = i0 + k * kReduceWarps;
+            mi[k] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) x[k][v] = 0.f;
+            if (i < nparts) {
+                mi[k] = ml[i];
+                if constexpr (VEC == 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(o + (int64_t)i * D);
+                    x[k][0] = t.x;
+                    x[k][1] = t.y;
+                    x[k][2] = t.z;
+                    x[k][3] = t.w;
+                } else {
+                    const float2 t = *reinterpret_cast<const float2 *>(o + (int64_t)i * D);
+                    x[k][0] = t.x;
+                    x[k][1] = t.y;
+                }
+            }
         }
+        float mb = m;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, mi[k].x);
+        if (mb == -INFINITY) continue;          // nothing visible yet
+        const float a = fast_exp2(m - mb);      // m = -inf (nothing yet): 0
+        l *= a;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) acc[v] *= a;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const float c = mi[k].x == -INFINITY ? 0.f : fast_exp2(mi[k].x - mb);
+            l = fmaf(mi[k].y, c, l);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc[v] = fmaf(x[k][v], c, acc[v]);
+        }
+        m = mb;
+    }
+    // the warps' results: M = the largest m, each warp's l and output scaled by 2^(m_w - M)
+    if (lane == 0) {
+        ml_s[2 * warp] = m;
+        ml_s[2 * warp + 1] = l;
     }
 #pragma unroll
     for (int v = 0; v < VEC; ++v) part_sum[warp * 128 + lane * VEC + v] = acc[v];
     __syncthreads();
     if (threadIdx.x < D) {
-        float t = 0.f;
+        float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kReduceWarps; ++w) t += part_sum[w * 128 + threadIdx.x];
-        reinterpret_cast<T *>(p.out)[((int64_t)b * p.num_heads + h) * D + threadIdx.x] = Elem<T>::from_f(t);
+        for (int w = 0; w < kReduceWarps; ++w) M = fmaxf(M, ml_s[2 * w]);
+        float t = 0.f, L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kReduceWarps; ++w) {
+            const float mw = ml_s[2 * w];
+            const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+            L = fmaf(ml_s[2 * w + 1], f, L);
+            t = fmaf(part_sum[w * 128 + threadIdx.x], f, t);
+        }
+        reinterpret_cast<T *>(p.out)[((int64_t)b * p.num_heads + h) * D + threadIdx.x] = Elem<T>::from_f(t / L);
     }
 }
 
@@ -446,7 +473,7 @@ __global__ __launch_bounds__(kReduceThreads) void decode_reduce_kernel(const Dec
     // a no-op unless launched as a programmatic dependent of the partition kernel
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ __align__(16) float part_sum[kReduceWarps * 128];
-    __shared__ float ml_s[2];
+    __shared__ float ml_s[2 * kReduceWarps];
     const int h = blockIdx.x, b = blockIdx.y;
     const SeqSplit sp = seq_split(p, b);
     if (sp.direct) return;                      // the partition kernel wrote the row
