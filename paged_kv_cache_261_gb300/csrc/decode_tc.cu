@@ -482,8 +482,8 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         // An item's finish (its last tile's O, the sum of l over the warps, the output)
         // is deferred until the next item's first tile has been through the softmax, so
         // the warpgroup does not wait for the last P.V at every item boundary: this is
-        // the item waiting for it. Measured per instance: long context (G = 8) 0.3925 ->
-        // 0.3898 ms, the sharing-aware batch's joining pass (G = 4) 0.0698 -> 0.0690 ms,
+        // the item waiting for it. Measured per instance: long context (G = 8) 0.3955 ->
+        // 0.3933 ms, the sharing-aware batch's joining pass (G = 4) 0.0699 -> 0.0690 ms,
         // but the 8B-shaped batch (G = 4) 0.0931 -> 0.0943 ms; the other instances
         // finish each item at its end.
         constexpr bool kDefer = kFold || GT == 8;
